@@ -1,0 +1,345 @@
+// Host side of the C ABI declared in include/hs.h: pool allocation,
+// argument checks, launches, counters and the link probe.
+#include <algorithm>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <random>
+#include <vector>
+
+#include "hs.h"
+#include "hs_internal.cuh"
+
+struct hs_pool {
+    hs_pool_desc desc;
+    std::vector<int32_t> anchor;
+    int device = 0;
+    int sm_count = 0;
+    int cluster_override = 0;
+    void *host = nullptr;
+    size_t host_bytes = 0;
+    hs::DevPool dp = {};
+    size_t cache_bytes = 0, pt_bytes = 0, meta_pairs = 0;
+};
+
+namespace {
+
+bool cuda_ok(cudaError_t e) { return e == cudaSuccess; }
+
+void free_device(hs_pool *p) {
+    cudaFree(p->dp.cache);
+    cudaFree(p->dp.pt);
+    cudaFree(p->dp.slot_pos);
+    cudaFree(p->dp.stamp);
+    cudaFree(p->dp.lru);
+    cudaFree(p->dp.tcount);
+    cudaFree(p->dp.busy);
+    cudaFree(p->dp.counters);
+    cudaFree(p->dp.status);
+    if (p->host) cudaFreeHost(p->host);
+    p->host = nullptr;
+}
+
+int reset_state(hs_pool *p) {
+    const size_t pairs = p->meta_pairs;
+    const size_t B = (size_t)p->desc.slots;
+    if (!cuda_ok(cudaMemset(p->dp.pt, 0xFF, p->pt_bytes)) ||
+        !cuda_ok(cudaMemset(p->dp.slot_pos, 0xFF, pairs * B * 4)) ||
+        !cuda_ok(cudaMemset(p->dp.stamp, 0, pairs * B * 4)) ||
+        !cuda_ok(cudaMemset(p->dp.tcount, 0, pairs * 4)) ||
+        !cuda_ok(cudaMemset(p->dp.busy, 0, pairs * 4)) ||
+        !cuda_ok(cudaMemset(p->dp.counters, 0, (size_t)p->desc.n_layers * hs::CTR_COUNT * 8)) ||
+        !cuda_ok(cudaMemset(p->dp.status, 0, 4)) ||
+        !cuda_ok(hs::launch_init_lru(p->dp.lru, (int64_t)pairs, (int)B, 0)) ||
+        !cuda_ok(cudaDeviceSynchronize()))
+        return HS_ERR_CUDA;
+    return HS_OK;
+}
+
+// Cluster size for a resolve over n_req requests: the largest power of two
+// up to 8 that keeps the grid within about two CTAs per SM.
+int pick_cluster(const hs_pool *p, int n_req) {
+    if (p->cluster_override > 0) return p->cluster_override;
+    int c = hs::kMaxCluster;
+    while (c > 1 && (int64_t)n_req * c > 2 * (int64_t)p->sm_count) c >>= 1;
+    return c;
+}
+
+bool check_common(const hs_pool *p, int32_t layer, int32_t n_req, int32_t k) {
+    return p && layer >= 0 && layer < p->desc.n_layers && n_req >= 0 &&
+           n_req <= p->desc.n_requests && k >= 1 && k <= p->desc.max_k;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *hs_strerror(int code) {
+    switch (code) {
+        case HS_OK: return "ok";
+        case HS_ERR_INVALID_ARG: return "invalid argument";
+        case HS_ERR_CUDA: return "CUDA runtime error";
+        case HS_ERR_NOMEM: return "out of memory or over the configured host limit";
+        case HS_ERR_DEVICE_INPUT: return "a kernel flagged invalid device input";
+        case HS_ERR_TIMEOUT: return "timeout";
+        case HS_ERR_UNSUPPORTED: return "sizes not supported by this build";
+        default: return "unknown error";
+    }
+}
+
+int32_t hs_kernels_per_call(void) { return 1; }
+
+size_t hs_plan_bytes(int32_t n_req, int32_t k) {
+    if (n_req < 0 || k < 0) return 0;
+    return hs::plan_bytes(n_req, k);
+}
+
+int hs_create_pool(const hs_pool_desc *desc, hs_pool **out) {
+    if (!out) return HS_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!desc) return HS_ERR_INVALID_ARG;
+    const hs_pool_desc d = *desc;
+    if (d.n_requests < 1 || d.n_layers < 1 || d.n_positions < 1 ||
+        d.n_positions > INT32_MAX || d.record_bytes < 16 || d.record_bytes % 16 != 0 ||
+        d.slots < 1 || d.slots > 32767 || d.max_k < 1 || d.max_k > d.slots)
+        return HS_ERR_INVALID_ARG;
+    // index arithmetic limits of the kernels (32-bit chunk counters and
+    // published row indices)
+    if ((int64_t)d.n_requests * d.slots > INT32_MAX ||
+        (int64_t)2 * d.max_k * (d.record_bytes / 16) > INT32_MAX / 2)
+        return HS_ERR_UNSUPPORTED;
+    if (d.layer_anchor) {
+        for (int l = 0; l < d.n_layers; ++l) {
+            const int a = d.layer_anchor[l];
+            if (a < 0 || a > l || d.layer_anchor[a] != a) return HS_ERR_INVALID_ARG;
+        }
+    }
+    const size_t host_bytes = (size_t)d.n_requests * d.n_layers * (size_t)d.n_positions * d.record_bytes;
+    if (d.host_limit_bytes && host_bytes > d.host_limit_bytes) return HS_ERR_NOMEM;
+
+    int dev = 0;
+    if (!cuda_ok(cudaGetDevice(&dev))) return HS_ERR_CUDA;
+    int smem_optin = 0, sms = 0;
+    if (!cuda_ok(cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) ||
+        !cuda_ok(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)))
+        return HS_ERR_CUDA;
+    const size_t need = hs::smem_layout(d.slots, d.max_k, true).total;
+    if (need > (size_t)smem_optin) return HS_ERR_UNSUPPORTED;
+
+    hs_pool *p = new (std::nothrow) hs_pool();
+    if (!p) return HS_ERR_NOMEM;
+    p->desc = d;
+    p->anchor.resize(d.n_layers);
+    for (int l = 0; l < d.n_layers; ++l) p->anchor[l] = d.layer_anchor ? d.layer_anchor[l] : l;
+    p->desc.layer_anchor = p->anchor.data();
+    p->device = dev;
+    p->sm_count = sms;
+    if (const char *e = std::getenv("HS_CLUSTER")) {
+        const int c = std::atoi(e);
+        if (c == 1 || c == 2 || c == 4 || c == 8) p->cluster_override = c;
+    }
+
+    const size_t pairs = (size_t)d.n_requests * d.n_layers;
+    const size_t B = (size_t)d.slots;
+    p->meta_pairs = pairs;
+    p->cache_bytes = pairs * B * d.record_bytes;
+    p->pt_bytes = pairs * (size_t)d.n_positions * 4;
+    p->host_bytes = host_bytes;
+
+    int rc = HS_OK;
+    void *hdev = nullptr;
+    if (!cuda_ok(cudaHostAlloc(&p->host, host_bytes, cudaHostAllocMapped | cudaHostAllocPortable))) {
+        p->host = nullptr;
+        rc = HS_ERR_NOMEM;
+        goto fail;
+    }
+    if (!cuda_ok(cudaHostGetDevicePointer(&hdev, p->host, 0))) { rc = HS_ERR_CUDA; goto fail; }
+    p->dp.host = static_cast<const uint8_t *>(hdev);
+    if (!cuda_ok(cudaMalloc(&p->dp.cache, p->cache_bytes)) ||
+        !cuda_ok(cudaMalloc(&p->dp.pt, p->pt_bytes)) ||
+        !cuda_ok(cudaMalloc(&p->dp.slot_pos, pairs * B * 4)) ||
+        !cuda_ok(cudaMalloc(&p->dp.stamp, pairs * B * 4)) ||
+        !cuda_ok(cudaMalloc(&p->dp.lru, pairs * B * 2)) ||
+        !cuda_ok(cudaMalloc(&p->dp.tcount, pairs * 4)) ||
+        !cuda_ok(cudaMalloc(&p->dp.busy, pairs * 4)) ||
+        !cuda_ok(cudaMalloc(&p->dp.counters, (size_t)d.n_layers * hs::CTR_COUNT * 8)) ||
+        !cuda_ok(cudaMalloc(&p->dp.status, 4))) {
+        cudaGetLastError();
+        rc = HS_ERR_NOMEM;
+        goto fail;
+    }
+    p->dp.R = d.n_requests;
+    p->dp.NL = d.n_layers;
+    p->dp.B = d.slots;
+    p->dp.W = d.record_bytes;
+    p->dp.L = d.n_positions;
+    if (!cuda_ok(hs::prepare_kernels(need))) { rc = HS_ERR_CUDA; goto fail; }
+    rc = reset_state(p);
+    if (rc != HS_OK) goto fail;
+    *out = p;
+    return HS_OK;
+fail:
+    free_device(p);
+    delete p;
+    return rc;
+}
+
+int hs_destroy_pool(hs_pool *pool) {
+    if (!pool) return HS_OK;
+    cudaDeviceSynchronize();
+    free_device(pool);
+    delete pool;
+    return HS_OK;
+}
+
+int hs_host_records(hs_pool *pool, int32_t req, int32_t layer, void **host_ptr) {
+    if (!pool || !host_ptr || req < 0 || req >= pool->desc.n_requests || layer < 0 ||
+        layer >= pool->desc.n_layers)
+        return HS_ERR_INVALID_ARG;
+    const size_t per = (size_t)pool->desc.n_positions * pool->desc.record_bytes;
+    *host_ptr = static_cast<uint8_t *>(pool->host) + ((size_t)req * pool->desc.n_layers + layer) * per;
+    return HS_OK;
+}
+
+int hs_device_views(hs_pool *pool, int32_t layer, hs_views *out) {
+    if (!pool || !out || layer < 0 || layer >= pool->desc.n_layers) return HS_ERR_INVALID_ARG;
+    const size_t R = pool->desc.n_requests, B = pool->desc.slots;
+    const size_t lp = (size_t)layer * R;
+    out->cache = pool->dp.cache + lp * B * pool->desc.record_bytes;
+    out->page_table = pool->dp.pt + lp * (size_t)pool->desc.n_positions;
+    out->slot_pos = pool->dp.slot_pos + lp * B;
+    out->stamps = pool->dp.stamp + lp * B;
+    out->lru = pool->dp.lru + lp * B;
+    out->resolves = pool->dp.tcount + lp;
+    return HS_OK;
+}
+
+int hs_resolve(hs_pool *pool, int32_t layer, int32_t n_req, const int32_t *d_req_ids,
+               const int32_t *d_sel, int32_t k, int32_t *d_out, const void *d_plan, void *stream) {
+    if (!check_common(pool, layer, n_req, k) || !d_sel || !d_out) return HS_ERR_INVALID_ARG;
+    if (d_plan && (reinterpret_cast<uintptr_t>(d_plan) & 15u)) return HS_ERR_INVALID_ARG;
+    if (n_req == 0) return HS_OK;
+    const cudaError_t e = hs::launch_resolve(pool->dp, layer, n_req, d_req_ids, d_sel, k, d_out, d_plan,
+                                             pick_cluster(pool, n_req), static_cast<cudaStream_t>(stream));
+    return cuda_ok(e) ? HS_OK : HS_ERR_CUDA;
+}
+
+int hs_prefetch_plan(hs_pool *pool, int32_t anchor_layer, int32_t target_layer, int32_t n_req,
+                     const int32_t *d_req_ids, const int32_t *d_sel, int32_t k, void *d_plan,
+                     void *stream) {
+    if (!check_common(pool, target_layer, n_req, k) || !d_sel || !d_plan) return HS_ERR_INVALID_ARG;
+    if (anchor_layer < 0 || anchor_layer >= pool->desc.n_layers ||
+        pool->anchor[target_layer] != anchor_layer)
+        return HS_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(d_plan) & 15u) return HS_ERR_INVALID_ARG;
+    if (n_req == 0) return HS_OK;
+    const cudaError_t e = hs::launch_plan(pool->dp, target_layer, n_req, d_req_ids, d_sel, k, d_plan,
+                                          static_cast<cudaStream_t>(stream));
+    return cuda_ok(e) ? HS_OK : HS_ERR_CUDA;
+}
+
+int hs_prefetch_copy(hs_pool *pool, int32_t target_layer, int32_t n_req, int32_t k,
+                     const void *d_plan, void *stream) {
+    if (!check_common(pool, target_layer, n_req, k) || !d_plan) return HS_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(d_plan) & 15u) return HS_ERR_INVALID_ARG;
+    if (n_req == 0) return HS_OK;
+    const cudaError_t e = hs::launch_prefetch_copy(pool->dp, target_layer, n_req, k, d_plan,
+                                                   pool->sm_count, static_cast<cudaStream_t>(stream));
+    return cuda_ok(e) ? HS_OK : HS_ERR_CUDA;
+}
+
+int hs_stats(hs_pool *pool, int32_t layer, hs_stats_t *out) {
+    if (!pool || !out || layer < -1 || layer >= pool->desc.n_layers) return HS_ERR_INVALID_ARG;
+    if (!cuda_ok(cudaDeviceSynchronize())) return HS_ERR_CUDA;
+    const int NL = pool->desc.n_layers;
+    std::vector<unsigned long long> c((size_t)NL * hs::CTR_COUNT);
+    uint32_t status = 0;
+    if (!cuda_ok(cudaMemcpy(c.data(), pool->dp.counters, c.size() * 8, cudaMemcpyDeviceToHost)) ||
+        !cuda_ok(cudaMemcpy(&status, pool->dp.status, 4, cudaMemcpyDeviceToHost)) ||
+        !cuda_ok(cudaMemset(pool->dp.status, 0, 4)))
+        return HS_ERR_CUDA;
+    std::memset(out, 0, sizeof(*out));
+    for (int l = 0; l < NL; ++l) {
+        if (layer >= 0 && l != layer) continue;
+        const unsigned long long *x = &c[(size_t)l * hs::CTR_COUNT];
+        out->resolves += x[hs::CTR_RESOLVES];
+        out->hits += x[hs::CTR_HITS];
+        out->misses += x[hs::CTR_MISSES];
+        out->fetched_bytes += x[hs::CTR_FETCHED];
+        out->prefetched_bytes += x[hs::CTR_PREFETCHED];
+        out->plan_hits += x[hs::CTR_PLAN_HITS];
+        out->plan_mismatches += x[hs::CTR_PLAN_MISMATCH];
+    }
+    out->status = status;
+    return status ? HS_ERR_DEVICE_INPUT : HS_OK;
+}
+
+int hs_reset(hs_pool *pool) {
+    if (!pool) return HS_ERR_INVALID_ARG;
+    if (!cuda_ok(cudaDeviceSynchronize())) return HS_ERR_CUDA;
+    return reset_state(pool);
+}
+
+int hs_link_probe(size_t bytes, int32_t reps, int32_t record_bytes, double *h2d_gbs,
+                  double *gather_gbs) {
+    if (bytes < (size_t)record_bytes || reps < 1 || record_bytes < 16 || record_bytes % 16)
+        return HS_ERR_INVALID_ARG;
+    const int64_t n_rec = (int64_t)(bytes / (size_t)record_bytes);
+    if (n_rec > INT32_MAX) return HS_ERR_INVALID_ARG;
+    bytes = (size_t)n_rec * record_bytes;
+    int dev = 0, sms = 0;
+    if (!cuda_ok(cudaGetDevice(&dev)) ||
+        !cuda_ok(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)))
+        return HS_ERR_CUDA;
+    void *hsrc = nullptr, *hsrc_dev = nullptr, *ddst = nullptr;
+    int32_t *didx = nullptr;
+    cudaStream_t st = nullptr;
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    int rc = HS_OK;
+    std::vector<int32_t> idx((size_t)n_rec);
+    if (!cuda_ok(cudaHostAlloc(&hsrc, bytes, cudaHostAllocMapped | cudaHostAllocPortable))) {
+        hsrc = nullptr;
+        return HS_ERR_NOMEM;
+    }
+    std::memset(hsrc, 0x5A, bytes);
+    for (int64_t i = 0; i < n_rec; ++i) idx[(size_t)i] = (int32_t)i;
+    std::shuffle(idx.begin(), idx.end(), std::mt19937_64(12345));
+    if (!cuda_ok(cudaHostGetDevicePointer(&hsrc_dev, hsrc, 0)) || !cuda_ok(cudaMalloc(&ddst, bytes)) ||
+        !cuda_ok(cudaMalloc(&didx, (size_t)n_rec * 4)) ||
+        !cuda_ok(cudaMemcpy(didx, idx.data(), (size_t)n_rec * 4, cudaMemcpyHostToDevice)) ||
+        !cuda_ok(cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking)) ||
+        !cuda_ok(cudaEventCreate(&e0)) || !cuda_ok(cudaEventCreate(&e1))) {
+        rc = HS_ERR_CUDA;
+        goto done;
+    }
+    for (int which = 0; which < 2; ++which) {
+        double *dst = which == 0 ? h2d_gbs : gather_gbs;
+        if (!dst) continue;
+        float best = 0.f;
+        for (int it = 0; it < reps + 1; ++it) {  // first run is a warm-up
+            cudaEventRecord(e0, st);
+            cudaError_t e = which == 0
+                                ? cudaMemcpyAsync(ddst, hsrc, bytes, cudaMemcpyHostToDevice, st)
+                                : hs::launch_gather_probe(static_cast<const uint8_t *>(hsrc_dev),
+                                                          static_cast<uint8_t *>(ddst), didx, n_rec,
+                                                          record_bytes, sms, st);
+            cudaEventRecord(e1, st);
+            if (!cuda_ok(e) || !cuda_ok(cudaEventSynchronize(e1))) { rc = HS_ERR_CUDA; goto done; }
+            float ms = 0.f;
+            cudaEventElapsedTime(&ms, e0, e1);
+            if (it > 0 && (best == 0.f || ms < best)) best = ms;
+        }
+        *dst = (double)bytes / (best * 1e-3) / 1e9;
+    }
+done:
+    if (e0) cudaEventDestroy(e0);
+    if (e1) cudaEventDestroy(e1);
+    if (st) cudaStreamDestroy(st);
+    cudaFree(didx);
+    cudaFree(ddst);
+    cudaFreeHost(hsrc);
+    return rc;
+}
+
+}  // extern "C"

@@ -1,0 +1,142 @@
+// Internal declarations shared by the CUDA translation units of libhs.
+//
+// Data layout in HBM (one pool, L = L_ctx, R requests, N_l layers, B slots,
+// W record bytes):
+//   cache    [N_l][R][B][W]  u8     layer-major, so a layer's cache is one
+//                                   [R*B][W] tensor and the published index
+//                                   r*B + slot is a row of it
+//   pt       [N_l][R][L]     i32    page table, -1 = host-only
+//   slot_pos [N_l][R][B]     i32    position held by each slot, -1 = empty
+//   stamp    [N_l][R][B]     u32    recency (0 empty, 2t-1 miss, 2t hit)
+//   lru      [N_l][R][B]     u16    slots sorted by (stamp, slot)
+//   tcount   [N_l][R]        u32    resolves done on the pair
+//   busy     [N_l][R]        u32    1 while a resolve owns the pair
+//   counters [N_l][8]        u64    see CTR_*
+//   status   [1]             u32    HS_STATUS_* bits
+// Host pool (pinned, device-mapped): host[R][N_l][L][W].
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace hs {
+
+constexpr int kThreads = 512;          // threads per CTA of every kernel
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxCluster = 8;         // portable cluster size limit
+constexpr uint32_t kPlanMagic = 0x4C505348u;  // "HSPL"
+
+enum Counter : int {
+    CTR_RESOLVES = 0,
+    CTR_HITS = 1,
+    CTR_MISSES = 2,
+    CTR_FETCHED = 3,
+    CTR_PREFETCHED = 4,
+    CTR_PLAN_HITS = 5,
+    CTR_PLAN_MISMATCH = 6,
+    CTR_COUNT = 8,
+};
+
+struct DevPool {
+    const uint8_t *host;  // device address of the mapped host pool
+    uint8_t *cache;
+    int32_t *pt;
+    int32_t *slot_pos;
+    uint32_t *stamp;
+    uint16_t *lru;
+    uint32_t *tcount;
+    uint32_t *busy;
+    unsigned long long *counters;
+    unsigned int *status;
+    int32_t R, NL, B, W;
+    int64_t L;
+};
+
+// Plan buffer: a 16-byte header {magic, n_req, k, layer}, then per request
+// i an entry of 16 + 8k bytes: {m, req, 0, 0}, pos[k], slot[k].
+struct PlanHeader {
+    uint32_t magic;
+    int32_t n_req, k, layer;
+};
+
+__host__ __device__ inline size_t plan_entry_bytes(int k) { return 16 + 8 * (size_t)k; }
+__host__ __device__ inline size_t plan_bytes(int n_req, int k) {
+    return 16 + (size_t)n_req * plan_entry_bytes(k);
+}
+
+__host__ __device__ inline int hash_capacity(int k) {
+    int h = 32;
+    while (h < 2 * k) h <<= 1;
+    return h;
+}
+
+__host__ __device__ inline uint32_t align16(uint32_t x) { return (x + 15u) & ~15u; }
+
+// Shared-memory layout of the resolve / plan kernels for (B, k).
+struct SmemLayout {
+    uint32_t hdr;      // header words + per-warp scan sums
+    uint32_t hash;     // u64[H]; after the probe it holds neworder u16[B]
+    uint32_t sel;      // i32[k]
+    uint32_t hit;      // i32[k]: slot of a hit, -1 before ranking, -2-rank for misses
+    uint32_t spos;     // i32[B]
+    uint32_t order;    // u16[B]
+    uint32_t flags;    // u8[B]: bit0 hit, bit1 victim
+    uint32_t vrank;    // u16[B]: rank of a victim slot among the victims
+    uint32_t mpos;     // i32[k]: miss positions by rank
+    uint32_t mslot;    // i32[k]: victims by rank
+    uint32_t fpos;     // i32[2k]: fetch list when a plan is consumed
+    uint32_t fslot;    // i32[2k]
+    uint32_t total;
+    int H;
+};
+
+__host__ __device__ inline SmemLayout smem_layout(int B, int k, bool with_plan) {
+    SmemLayout s;
+    uint32_t o = 0;
+    s.H = hash_capacity(k);
+    s.hdr = o;   o += 256;
+    s.hash = o;  { uint32_t a = 8u * s.H, b = 2u * B; o += align16(a > b ? a : b); }
+    s.sel = o;   o += align16(4u * k);
+    s.hit = o;   o += align16(4u * k);
+    s.spos = o;  o += align16(4u * B);
+    s.order = o; o += align16(2u * B);
+    s.flags = o; o += align16(1u * B);
+    s.vrank = o; o += align16(2u * B);
+    s.mpos = o;  o += align16(4u * k);
+    s.mslot = o; o += align16(4u * k);
+    s.fpos = o;  o += with_plan ? align16(8u * k) : 0;
+    s.fslot = o; o += with_plan ? align16(8u * k) : 0;
+    s.total = o;
+    return s;
+}
+
+// header word indices (u32 at smem + hdr)
+enum Hdr : int {
+    H_ABORT = 0,     // HS_STATUS_* bits that abort this request
+    H_M = 1,         // misses
+    H_NH = 2,        // non-hit slots
+    H_F = 3,         // entries in the fetch list
+    H_FLIST = 4,     // 0: fetch list = (mpos, mslot); 1: (fpos, fslot)
+    H_T = 5,         // this resolve's t
+    H_NF = 6,        // atomic fill counter of the plan-mode fetch list
+    H_PMISS = 7,     // plan-mode mismatches
+    H_PHIT = 8,      // plan-mode plan hits
+    H_SUMS = 16,     // kWarps scan sums from here
+};
+
+// launchers (resolve.cu, copy.cu)
+cudaError_t launch_resolve(const DevPool &p, int layer, int n_req, const int32_t *req_ids,
+                           const int32_t *sel, int k, int32_t *out, const void *plan,
+                           int cluster, cudaStream_t st);
+cudaError_t launch_plan(const DevPool &p, int layer, int n_req, const int32_t *req_ids,
+                        const int32_t *sel, int k, void *plan, cudaStream_t st);
+cudaError_t launch_prefetch_copy(const DevPool &p, int layer, int n_req, int k,
+                                 const void *plan, int sm_count, cudaStream_t st);
+cudaError_t launch_init_lru(uint16_t *lru, int64_t pairs, int B, cudaStream_t st);
+cudaError_t prepare_kernels(size_t max_smem);
+cudaError_t launch_gather_probe(const uint8_t *src, uint8_t *dst, const int32_t *idx,
+                                int64_t n_rec, int W, int sm_count, cudaStream_t st);
+
+}  // namespace hs

@@ -1,0 +1,227 @@
+"""Thin Python binding of the C ABI in ``include/hs.h``.
+
+Functions carry the C names and only marshal arguments: every step of the
+resolve path runs in the CUDA kernels of ``libhs.so``.  Device buffers may be
+passed as torch tensors (their ``data_ptr()`` is used) or as raw integer
+addresses; streams as ``torch.cuda.Stream`` objects, raw handles, or ``None``
+for torch's current stream.  A failing call raises :class:`HsError`.
+
+:class:`Pool` wraps a pool handle with numpy views of the host records and
+zero-copy torch views of the device metadata.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+
+from . import _native
+
+HS_OK = 0
+HS_ERR_INVALID_ARG = -1
+HS_ERR_CUDA = -2
+HS_ERR_NOMEM = -3
+HS_ERR_DEVICE_INPUT = -4
+HS_ERR_TIMEOUT = -5
+HS_ERR_UNSUPPORTED = -6
+
+HS_STATUS_POS_RANGE = 0x1
+HS_STATUS_POS_DUP = 0x2
+HS_STATUS_REQ_RANGE = 0x4
+HS_STATUS_REQ_BUSY = 0x8
+HS_STATUS_PLAN = 0x10
+HS_STATUS_META = 0x20
+
+
+class HsError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {hs_strerror(code)} ({code})")
+
+
+def _lib():
+    return _native.load()
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != HS_OK:
+        raise HsError(rc, what)
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    if isinstance(x, np.ndarray):
+        return x.ctypes.data
+    raise TypeError(f"cannot take the address of {type(x).__name__}")
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def hs_strerror(code: int) -> str:
+    return _lib().hs_strerror(code).decode()
+
+
+def hs_kernels_per_call() -> int:
+    return int(_lib().hs_kernels_per_call())
+
+
+def hs_plan_bytes(n_req: int, k: int) -> int:
+    return int(_lib().hs_plan_bytes(n_req, k))
+
+
+def hs_create_pool(n_requests, n_layers, n_positions, record_bytes, slots, max_k,
+                   layer_anchor=None, host_limit_bytes=0) -> int:
+    anchors = None
+    if layer_anchor is not None:
+        anchors = (ctypes.c_int32 * len(layer_anchor))(*layer_anchor)
+    d = _native.PoolDesc(n_requests, n_layers, n_positions, record_bytes, slots, max_k,
+                         ctypes.cast(anchors, ctypes.c_void_p) if anchors is not None else None,
+                         host_limit_bytes)
+    h = ctypes.c_void_p()
+    _check(_lib().hs_create_pool(ctypes.byref(d), ctypes.byref(h)), "hs_create_pool")
+    return h.value
+
+
+def hs_destroy_pool(pool: int) -> None:
+    _check(_lib().hs_destroy_pool(pool), "hs_destroy_pool")
+
+
+def hs_host_records(pool: int, req: int, layer: int) -> int:
+    p = ctypes.c_void_p()
+    _check(_lib().hs_host_records(pool, req, layer, ctypes.byref(p)), "hs_host_records")
+    return p.value
+
+
+def hs_device_views(pool: int, layer: int) -> _native.Views:
+    v = _native.Views()
+    _check(_lib().hs_device_views(pool, layer, ctypes.byref(v)), "hs_device_views")
+    return v
+
+
+def hs_resolve(pool, layer, n_req, req_ids, sel, k, out, plan=None, stream=None) -> None:
+    _check(_lib().hs_resolve(pool, layer, n_req, _ptr(req_ids), _ptr(sel), k, _ptr(out),
+                             _ptr(plan), _stream(stream)), "hs_resolve")
+
+
+def hs_prefetch_plan(pool, anchor_layer, target_layer, n_req, req_ids, sel, k, plan,
+                     stream=None) -> None:
+    _check(_lib().hs_prefetch_plan(pool, anchor_layer, target_layer, n_req, _ptr(req_ids),
+                                   _ptr(sel), k, _ptr(plan), _stream(stream)), "hs_prefetch_plan")
+
+
+def hs_prefetch_copy(pool, target_layer, n_req, k, plan, stream=None) -> None:
+    _check(_lib().hs_prefetch_copy(pool, target_layer, n_req, k, _ptr(plan), _stream(stream)),
+           "hs_prefetch_copy")
+
+
+def hs_stats(pool, layer: int = -1, check: bool = True) -> dict:
+    """Counters of `layer` (-1: all).  With check=False a status error is
+    returned in the dict instead of raised."""
+    s = _native.Stats()
+    rc = _lib().hs_stats(pool, layer, ctypes.byref(s))
+    if rc not in (HS_OK, HS_ERR_DEVICE_INPUT) or (check and rc != HS_OK):
+        raise HsError(rc, f"hs_stats (status 0x{s.status:x})")
+    d = {f: int(getattr(s, f)) for f, _ in _native.Stats._fields_}
+    d["rc"] = rc
+    return d
+
+
+def hs_reset(pool) -> None:
+    _check(_lib().hs_reset(pool), "hs_reset")
+
+
+def hs_link_probe(nbytes: int, reps: int = 10, record_bytes: int = 1152):
+    """(H2D memcpy GB/s, scattered-record GPU-load GB/s), best of `reps`."""
+    a, b = ctypes.c_double(), ctypes.c_double()
+    _check(_lib().hs_link_probe(nbytes, reps, record_bytes, ctypes.byref(a), ctypes.byref(b)),
+           "hs_link_probe")
+    return a.value, b.value
+
+
+class _CudaArray:
+    def __init__(self, ptr, shape, typestr):
+        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr,
+                                         "data": (ptr, False), "version": 3, "strides": None}
+
+
+class Pool:
+    """A pool handle plus host and device views."""
+
+    def __init__(self, n_requests, n_layers, n_positions, record_bytes, slots, max_k,
+                 layer_anchor=None, host_limit_bytes=0):
+        self.R, self.NL, self.L = n_requests, n_layers, n_positions
+        self.W, self.B, self.max_k = record_bytes, slots, max_k
+        self.handle = hs_create_pool(n_requests, n_layers, n_positions, record_bytes, slots,
+                                     max_k, layer_anchor, host_limit_bytes)
+
+    @classmethod
+    def for_workload(cls, w, host_limit_bytes=0):
+        return cls(w.n_requests, w.n_layers, w.n_positions, w.record_bytes, w.slots, w.k,
+                   list(w.anchors), host_limit_bytes)
+
+    def close(self):
+        if self.handle:
+            hs_destroy_pool(self.handle)
+            self.handle = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def host_records(self, req, layer) -> np.ndarray:
+        """numpy uint8 view [L][W] of the pinned host records of (req, layer)."""
+        addr = hs_host_records(self.handle, req, layer)
+        buf = (ctypes.c_uint8 * (self.L * self.W)).from_address(addr)
+        return np.frombuffer(buf, np.uint8).reshape(self.L, self.W)
+
+    def views(self, layer):
+        """torch tensors (zero-copy) over the device arrays of `layer`."""
+        import torch
+        v = hs_device_views(self.handle, layer)
+        R, B, L, W = self.R, self.B, self.L, self.W
+
+        def t(ptr, shape, ts):
+            return torch.as_tensor(_CudaArray(ptr, shape, ts), device="cuda")
+        return {"cache": t(v.cache, (R * B, W), "|u1"),
+                "page_table": t(v.page_table, (R, L), "<i4"),
+                "slot_pos": t(v.slot_pos, (R, B), "<i4"),
+                "stamps": t(v.stamps, (R, B), "<u4"),
+                "lru": t(v.lru, (R, B), "<u2"),
+                "resolves": t(v.resolves, (R,), "<u4")}
+
+    def resolve(self, layer, sel, out, req_ids=None, plan=None, stream=None, n_req=None):
+        n = sel.shape[0] if n_req is None else n_req
+        hs_resolve(self.handle, layer, n, req_ids, sel, sel.shape[-1], out, plan, stream)
+
+    def prefetch_plan(self, anchor_layer, target_layer, sel, plan, req_ids=None, stream=None):
+        hs_prefetch_plan(self.handle, anchor_layer, target_layer, sel.shape[0], req_ids, sel,
+                         sel.shape[-1], plan, stream)
+
+    def prefetch_copy(self, target_layer, n_req, k, plan, stream=None):
+        hs_prefetch_copy(self.handle, target_layer, n_req, k, plan, stream)
+
+    def stats(self, layer=-1, check=True):
+        return hs_stats(self.handle, layer, check)
+
+    def reset(self):
+        hs_reset(self.handle)

@@ -1,0 +1,232 @@
+/*
+ * hs.h -- C ABI of a GB300-native RESOLVE step for a two-level KV cache.
+ *
+ * The method (HiSparse, "Scaling Sparse-Attention Decoding with Hierarchical
+ * KV Cache Management"; described in "Inference Systems Infrastructure Notes
+ * (6): HiSparse" and in the Pith review of arXiv 2608.07009):
+ *
+ *  - every KV record lives in a pinned, device-mapped host pool, addressed
+ *    contiguously by logical position; it is the only authoritative copy
+ *    (notes, section 2 "Two-Level Hierarchy", items 1 and 2.1.2);
+ *  - each (request, layer) pair owns B >= k GPU slots, a page table over the
+ *    L_ctx positions (slot or host-only) and per-slot recency for LRU
+ *    (notes, section 2, items 2 and 3);
+ *  - one fused RESOLVE launch per sparse layer and decode step turns the k
+ *    selected positions of every request into physical slot indices,
+ *    fetching misses from host memory with GPU-thread loads (notes,
+ *    section 3 "RESOLVE: Five Stages in One Launch"; Pith review, "What
+ *    carries the argument");
+ *  - for layers that share an anchor layer's selection, the misses are
+ *    known before the layer runs: a plan is computed and replayed by a
+ *    copy-only kernel on a side stream (notes, section 4 "Exact Layer-Wise
+ *    Prefetching").
+ *
+ * Conventions
+ *  - Every call returns an int: HS_OK (0) or a negative HS_ERR_* code.
+ *  - hs_resolve, hs_prefetch_plan and hs_prefetch_copy only enqueue work on
+ *    the given stream: they never synchronise, never allocate, and can be
+ *    captured in a CUDA graph when their arguments stay fixed.
+ *  - Errors in device-resident inputs (a position outside [0, L_ctx), a
+ *    repeated position, a request id outside the pool, a request resolved
+ *    twice at once, a malformed plan) never trap the GPU.  The kernel sets a
+ *    bit in the pool's status word (HS_STATUS_*), publishes -1 for the whole
+ *    request and leaves that request's metadata and slots untouched;
+ *    hs_stats reports the bits and returns HS_ERR_DEVICE_INPUT.
+ *  - Ownership: the pool owns the host pool and every device array it
+ *    allocates; callers own selections, outputs, plans and streams.
+ *  - Ordering: two operations on the same layer must not overlap on the GPU.
+ *    A resolve that consumes a plan must be ordered after the
+ *    hs_prefetch_copy of that plan (an event between the streams).
+ *  - One device: the pool lives on the device current at hs_create_pool;
+ *    every later call must run with that device current.
+ */
+#ifndef HS_H
+#define HS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- return codes ------------------------------------------------------ */
+#define HS_OK 0
+#define HS_ERR_INVALID_ARG (-1)   /* bad descriptor, index, size or pointer */
+#define HS_ERR_CUDA (-2)          /* a CUDA runtime call failed */
+#define HS_ERR_NOMEM (-3)         /* allocation refused or over the limit */
+#define HS_ERR_DEVICE_INPUT (-4)  /* a kernel flagged bad device input (hs_stats) */
+#define HS_ERR_TIMEOUT (-5)       /* reserved: no call waits on the GPU with a limit */
+#define HS_ERR_UNSUPPORTED (-6)   /* sizes beyond what this build's kernels handle */
+
+/* ---- bits of the device status word (hs_stats_t.status) ---------------- */
+#define HS_STATUS_POS_RANGE 0x1u  /* a selected position outside [0, L_ctx) */
+#define HS_STATUS_POS_DUP 0x2u    /* a position selected twice in one request */
+#define HS_STATUS_REQ_RANGE 0x4u  /* a request id outside [0, n_requests) */
+#define HS_STATUS_REQ_BUSY 0x8u   /* a request resolved by two overlapping calls */
+#define HS_STATUS_PLAN 0x10u      /* a plan that does not belong to this call */
+#define HS_STATUS_META 0x20u      /* slot map or LRU order found corrupted */
+
+/* Opaque pool: host records, GPU slots and metadata of every
+ * (request, layer) pair.  Library-owned. */
+typedef struct hs_pool hs_pool;
+
+typedef struct {
+    int32_t n_requests;   /* R: request rows in the pool (>= 1) */
+    int32_t n_layers;     /* N_l: sparse layers (>= 1) */
+    int64_t n_positions;  /* L_ctx: logical positions per request (1 .. 2^31-1) */
+    int32_t record_bytes; /* W = W_KV * s: bytes per KV record, a multiple of 16 */
+    int32_t slots;        /* B: GPU slots per (request, layer) (1 .. 32767) */
+    int32_t max_k;        /* largest k passed to hs_resolve (1 .. slots) */
+    /* layer_anchor[l]: the layer whose selection layer l shares (l itself for
+       an anchor).  May be NULL (every layer its own anchor).  Copied. */
+    const int32_t *layer_anchor;
+    /* Refuse pools whose pinned host pool would exceed this many bytes
+       (0: no limit beyond what the system grants).  HS_ERR_NOMEM. */
+    uint64_t host_limit_bytes;
+} hs_pool_desc;
+
+typedef struct {
+    uint64_t resolves;          /* resolves committed (one per request per call) */
+    uint64_t hits;              /* selected positions found resident */
+    uint64_t misses;            /* selected positions fetched into a victim slot */
+    uint64_t fetched_bytes;     /* bytes the resolve kernel copied from host */
+    uint64_t prefetched_bytes;  /* bytes hs_prefetch_copy copied from host */
+    uint64_t plan_hits;         /* misses whose copy a plan had already done */
+    uint64_t plan_mismatches;   /* plan pairs or misses that did not match */
+    uint32_t status;            /* HS_STATUS_* bits since the last hs_stats */
+} hs_stats_t;
+
+/* Device views of one layer, for the attention consumer and for checks.
+ * Layout: the layer's cache is [n_requests * slots][record_bytes] bytes, so
+ * a published index i addresses row i; the other arrays are
+ * [n_requests][...] row-major. */
+typedef struct {
+    void *cache;          /* [R*B][W] slot contents (HBM) */
+    int32_t *page_table;  /* [R][L_ctx] slot of each position, -1 = host-only */
+    int32_t *slot_pos;    /* [R][B] position held by each slot, -1 = empty */
+    uint32_t *stamps;     /* [R][B] recency: 0 empty, 2t-1 filled at the t-th
+                             resolve of the pair, 2t hit at the t-th resolve */
+    uint16_t *lru;        /* [R][B] slots in ascending (stamp, slot) order */
+    uint32_t *resolves;   /* [R] resolves done on each pair (t) */
+} hs_views;
+
+/*
+ * Creates a pool: allocates the pinned, device-mapped host pool
+ * (R * N_l * L_ctx * W bytes, host[r][l][pos][W], left uninitialised) and
+ * the device arrays: cache (N_l * R * B * W bytes), page tables
+ * (N_l * R * L_ctx * 4 bytes), slot maps, stamps, LRU orders, counters.
+ * All slots start empty, every page-table entry host-only, every stamp 0.
+ * The device-side footprint of KV records per request is N_l * B * W
+ * bytes whatever L_ctx is (notes, section 2, "HBM usage = N_l x B x W_KV x s").
+ * Errors: HS_ERR_INVALID_ARG (desc fields out of range, out == NULL),
+ * HS_ERR_NOMEM (over host_limit_bytes or an allocation failed),
+ * HS_ERR_UNSUPPORTED (B or max_k needs more shared memory than a CTA has),
+ * HS_ERR_CUDA.  On error *out is NULL and nothing stays allocated.
+ */
+int hs_create_pool(const hs_pool_desc *desc, hs_pool **out);
+
+/* Synchronises the device, then frees everything the pool owns.
+ * NULL is accepted and ignored. */
+int hs_destroy_pool(hs_pool *pool);
+
+/* Host address of the records of (req, layer): L_ctx * W bytes, record
+ * `pos` at byte offset pos * W.  The caller (prefill, a generator) writes
+ * them before the first resolve that can select them and must not change a
+ * record while a kernel may read it. */
+int hs_host_records(hs_pool *pool, int32_t req, int32_t layer, void **host_ptr);
+
+/* Device views of `layer` (see hs_views). */
+int hs_device_views(hs_pool *pool, int32_t layer, hs_views *out);
+
+/*
+ * RESOLVE for one sparse layer: for each of the n_req requests
+ * r = d_req_ids[i] (or r = i when d_req_ids is NULL), given its k selected
+ * positions d_sel[i][0..k), one fused launch
+ *   1. builds a shared-memory hash table over the selected positions,
+ *   2. probes every slot's position against it to mark hits,
+ *   3. gives the j-th miss (selection order) the j-th victim, victims being
+ *      the non-hit slots in ascending (stamp, slot) order,
+ *   4. copies each missed record from the host pool into its victim slot
+ *      with 16-byte non-coherent GPU-thread loads,
+ *   5. updates page table, slot map, stamps (misses 2t-1, hits 2t) and LRU
+ *      order, and writes d_out[i][j] = r * B + slot of d_sel[i][j].
+ * (notes, section 3; Pith review, "What carries the argument".)
+ * d_req_ids: device int32[n_req] or NULL; ids must be distinct.
+ * d_sel: device int32[n_req][k]; d_out: device int32[n_req][k].
+ * d_plan: NULL, or a plan made by hs_prefetch_plan for this layer with the
+ *   same n_req, request ids, selection and k, already copied by
+ *   hs_prefetch_copy: misses the plan covered are not copied again; any plan
+ *   pair that is not exactly this resolve's own is re-fetched, so the result
+ *   is the same with or without a plan.  16-byte aligned.
+ * n_req == 0 enqueues nothing.  Errors: HS_ERR_INVALID_ARG (layer, n_req > R,
+ * k outside [1, max_k], NULL d_sel/d_out), HS_ERR_CUDA (launch failed).
+ */
+int hs_resolve(hs_pool *pool, int32_t layer, int32_t n_req, const int32_t *d_req_ids,
+               const int32_t *d_sel, int32_t k, int32_t *d_out, const void *d_plan,
+               void *stream);
+
+/* Bytes of a plan buffer for n_req requests of k selections. */
+size_t hs_plan_bytes(int32_t n_req, int32_t k);
+
+/*
+ * Exact layer-wise prefetch, plan half: runs steps 1-3 of hs_resolve for
+ * target_layer against that layer's own current metadata, read-only, with
+ * the anchor layer's selection d_sel, and writes the (position, victim)
+ * pairs of every request into d_plan (hs_plan_bytes(n_req, k) bytes,
+ * 16-byte aligned).  For a layer whose history matches its anchor's, the
+ * plan is the anchor's miss plan (notes, section 4).  target_layer must
+ * share anchor_layer's selection (desc.layer_anchor); the metadata of
+ * target_layer must not change between this call and the resolve that
+ * consumes the plan.  Errors as hs_resolve.
+ */
+int hs_prefetch_plan(hs_pool *pool, int32_t anchor_layer, int32_t target_layer,
+                     int32_t n_req, const int32_t *d_req_ids, const int32_t *d_sel,
+                     int32_t k, void *d_plan, void *stream);
+
+/*
+ * Exact layer-wise prefetch, copy half: a copy-only kernel that writes
+ * host[r][target_layer][pos] into slot `slot` of request r for every pair of
+ * d_plan (n_req, k as given to hs_prefetch_plan).  Meant for a side stream
+ * so that the transfer overlaps other work (notes, section 4).  It touches
+ * no metadata: the consuming hs_resolve commits it.
+ */
+int hs_prefetch_copy(hs_pool *pool, int32_t target_layer, int32_t n_req, int32_t k,
+                     const void *d_plan, void *stream);
+
+/*
+ * Synchronises the device, then reports the counters of `layer` (-1: the
+ * sum over all layers) and the status word, and clears the status word.
+ * Returns HS_ERR_DEVICE_INPUT when a status bit was set (the counters are
+ * still filled in).  Not callable during stream capture.
+ */
+int hs_stats(hs_pool *pool, int32_t layer, hs_stats_t *out);
+
+/* Synchronises, then empties every slot of every pair (as after
+ * hs_create_pool) and zeroes the counters; the host records are kept. */
+int hs_reset(hs_pool *pool);
+
+/*
+ * Link ceiling probe (not part of the hot path).  Allocates `bytes` of
+ * pinned host memory and the same on the device, then reports the best of
+ * `reps` timed runs (CUDA events) of
+ *   *h2d_gbs:    cudaMemcpyAsync host -> device of the whole buffer;
+ *   *gather_gbs: a kernel that copies `bytes` worth of record_bytes-sized
+ *                records from random record indices of the pinned buffer
+ *                into device memory with 16-byte GPU-thread loads.
+ * Either output pointer may be NULL.  Frees what it allocated.
+ */
+int hs_link_probe(size_t bytes, int32_t reps, int32_t record_bytes, double *h2d_gbs,
+                  double *gather_gbs);
+
+/* Kernels launched per call of hs_resolve / hs_prefetch_plan /
+ * hs_prefetch_copy (for launch accounting; always 1 in this build). */
+int32_t hs_kernels_per_call(void);
+
+/* Static description of an error code. */
+const char *hs_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* HS_H */

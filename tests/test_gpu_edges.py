@@ -1,0 +1,286 @@
+"""Edge cases of the GPU path, each against the CPU oracle or a fixed fact."""
+import numpy as np
+import pytest
+import torch
+
+from hierarchical_kv_cache_resolve_gb300 import hs
+from oracle.oracle import OK, Pair
+from tests.gpu_harness import check_cache, check_metadata, fill_selected
+from workloads import configs, records
+
+pytestmark = pytest.mark.gpu
+
+
+def _small(**kw):
+    base = dict(n_requests=3, n_layers=2, n_positions=3000, record_bytes=144, slots=96,
+                k=40, steps=10)
+    base.update(kw)
+    return configs.TINY.with_(**base)
+
+
+def _random_trace(w, seed=0):
+    rng = np.random.default_rng(seed)
+    sel = np.empty((w.steps, w.n_requests, w.n_layers, w.k), np.int32)
+    for t in range(w.steps):
+        for r in range(w.n_requests):
+            for l in range(w.n_layers):
+                sel[t, r, l] = rng.choice(w.n_positions, w.k, replace=False)
+    return sel
+
+
+def _oracles(w):
+    return {(r, l): Pair(w.slots, w.n_positions, w.record_bytes)
+            for r in range(w.n_requests) for l in range(w.n_layers)}
+
+
+def test_bad_positions_abort_only_their_request():
+    w = _small()
+    sel = _random_trace(w)
+    orc = _oracles(w)
+    with hs.Pool.for_workload(w) as pool:
+        fill_selected(pool, w, sel)
+        out = torch.empty((w.n_requests, w.k), dtype=torch.int32, device="cuda")
+        for t in range(3):
+            s = torch.from_numpy(np.ascontiguousarray(sel[t, :, 0])).cuda()
+            pool.resolve(0, s, out)
+            for r in range(w.n_requests):
+                orc[(r, 0)].resolve(sel[t, r, 0], out_base=r * w.slots)
+        before = {r: (pool.views(0)["slot_pos"][r].cpu().numpy(),
+                      pool.views(0)["page_table"][r].cpu().numpy()) for r in range(w.n_requests)}
+        for bad, bit in (("dup", hs.HS_STATUS_POS_DUP), ("range", hs.HS_STATUS_POS_RANGE),
+                         ("neg", hs.HS_STATUS_POS_RANGE)):
+            s = sel[3, :, 0].copy()
+            if bad == "dup":
+                s[1, 7] = s[1, 3]
+            elif bad == "range":
+                s[1, 0] = w.n_positions
+            else:
+                s[1, 5] = -3
+            pool.resolve(0, torch.from_numpy(s).cuda(), out)
+            st = pool.stats(0, check=False)
+            assert st["rc"] == hs.HS_ERR_DEVICE_INPUT and st["status"] & bit
+            got = out.cpu().numpy()
+            assert (got[1] == -1).all()
+            for r in (0, 2):
+                rc, o, _ = orc[(r, 0)].resolve(s[r], out_base=r * w.slots)
+                assert rc == OK and np.array_equal(got[r], o)
+            assert np.array_equal(pool.views(0)["slot_pos"][1].cpu().numpy(), before[1][0])
+            assert np.array_equal(pool.views(0)["page_table"][1].cpu().numpy(), before[1][1])
+        assert pool.stats(0)["status"] == 0   # cleared by the previous read
+        for r in range(w.n_requests):
+            check_metadata(pool, w, 0, r, orc[(r, 0)], int(orc[(r, 0)].t[0]))
+
+
+def test_bad_request_ids_and_empty_call():
+    w = _small()
+    sel = _random_trace(w)
+    with hs.Pool.for_workload(w) as pool:
+        fill_selected(pool, w, sel)
+        out = torch.full((2, w.k), 7, dtype=torch.int32, device="cuda")
+        ids = torch.tensor([2, w.n_requests], dtype=torch.int32, device="cuda")
+        s = torch.from_numpy(np.ascontiguousarray(sel[0, [2, 0], 1])).cuda()
+        pool.resolve(1, s, out, req_ids=ids)
+        st = pool.stats(1, check=False)
+        assert st["status"] & hs.HS_STATUS_REQ_RANGE
+        got = out.cpu().numpy()
+        assert (got[1] == -1).all()
+        p = Pair(w.slots, w.n_positions, w.record_bytes)
+        rc, o, _ = p.resolve(sel[0, 2, 1], out_base=2 * w.slots)
+        assert np.array_equal(got[0], o)
+        # n_req = 0 enqueues nothing
+        hs.hs_resolve(pool.handle, 1, 0, None, s, w.k, out)
+        assert pool.stats(1)["resolves"] == 1
+
+
+def test_permuted_request_subsets():
+    w = _small(n_requests=6, steps=12)
+    sel = _random_trace(w, seed=5)
+    orc = _oracles(w)
+    rng = np.random.default_rng(11)
+    with hs.Pool.for_workload(w) as pool:
+        fill_selected(pool, w, sel)
+        for t in range(w.steps):
+            for l in range(w.n_layers):
+                ids = rng.permutation(w.n_requests)[: rng.integers(1, w.n_requests + 1)]
+                s = torch.from_numpy(np.ascontiguousarray(sel[t, ids, l])).cuda()
+                out = torch.empty((ids.size, w.k), dtype=torch.int32, device="cuda")
+                pool.resolve(l, s, out, req_ids=torch.from_numpy(ids.astype(np.int32)).cuda())
+                got = out.cpu().numpy()
+                for i, r in enumerate(ids):
+                    rc, o, _ = orc[(r, l)].resolve(sel[t, r, l], out_base=r * w.slots)
+                    assert rc == OK and np.array_equal(got[i], o)
+        for (r, l), p in orc.items():
+            check_metadata(pool, w, l, r, p, int(p.t[0]))
+            check_cache(pool, w, l, r, p.slot_pos)
+
+
+@pytest.mark.parametrize("shape", [dict(k=96, slots=96), dict(k=1, slots=96),
+                                   dict(k=40, slots=64, n_positions=50),
+                                   dict(k=33, slots=33, record_bytes=16),
+                                   dict(k=64, slots=200, record_bytes=4096)])
+def test_shapes(shape):
+    w = _small(**shape)
+    sel = _random_trace(w, seed=3)
+    orc = _oracles(w)
+    with hs.Pool.for_workload(w) as pool:
+        fill_selected(pool, w, sel)
+        out = torch.empty((w.n_requests, w.k), dtype=torch.int32, device="cuda")
+        for t in range(w.steps):
+            for l in range(w.n_layers):
+                pool.resolve(l, torch.from_numpy(np.ascontiguousarray(sel[t, :, l])).cuda(), out)
+                got = out.cpu().numpy()
+                for r in range(w.n_requests):
+                    rc, o, _ = orc[(r, l)].resolve(sel[t, r, l], out_base=r * w.slots)
+                    assert rc == OK and np.array_equal(got[r], o)
+        for (r, l), p in orc.items():
+            check_metadata(pool, w, l, r, p, w.steps)
+            check_cache(pool, w, l, r, p.slot_pos)
+        if w.slots >= w.n_positions:
+            # the cache holds the whole context: no record is ever evicted
+            assert pool.stats()["misses"] == sum(
+                len(np.unique(sel[:, r, l])) for r in range(w.n_requests)
+                for l in range(w.n_layers))
+
+
+def test_largest_supported_slots_and_rejection():
+    w = _small(n_requests=2, n_layers=1, k=2048, slots=14000, n_positions=60000,
+               record_bytes=64, steps=6)
+    sel = _random_trace(w, seed=8)
+    orc = _oracles(w)
+    with hs.Pool.for_workload(w) as pool:
+        fill_selected(pool, w, sel)
+        out = torch.empty((w.n_requests, w.k), dtype=torch.int32, device="cuda")
+        for t in range(w.steps):
+            pool.resolve(0, torch.from_numpy(np.ascontiguousarray(sel[t, :, 0])).cuda(), out)
+            got = out.cpu().numpy()
+            for r in range(w.n_requests):
+                rc, o, _ = orc[(r, 0)].resolve(sel[t, r, 0], out_base=r * w.slots)
+                assert np.array_equal(got[r], o)
+        for r in range(w.n_requests):
+            check_metadata(pool, w, 0, r, orc[(r, 0)], w.steps)
+    with pytest.raises(hs.HsError) as e:
+        hs.Pool(1, 1, 100000, 64, 30000, 2048)
+    assert e.value.code == hs.HS_ERR_UNSUPPORTED
+
+
+def _run_group(pool, w, sel, plan_fn):
+    """Layer 0 anchors layers 1 and 2; plan_fn(t, layer, plan tensor) may
+    corrupt the plan between plan and copy."""
+    R, k = w.n_requests, w.k
+    out = torch.empty((3, R, k), dtype=torch.int32, device="cuda")
+    plan = torch.empty(hs.hs_plan_bytes(R, k), dtype=torch.uint8, device="cuda")
+    res = []
+    for t in range(w.steps):
+        s = torch.from_numpy(np.ascontiguousarray(sel[t, :, 0])).cuda()
+        pool.resolve(0, s, out[0])
+        for l in (1, 2):
+            if plan_fn is not None:
+                pool.prefetch_plan(0, l, s, plan)
+                plan_fn(t, l, plan)
+                pool.prefetch_copy(l, R, k, plan)
+                pool.resolve(l, s, out[l], plan=plan)
+            else:
+                pool.resolve(l, s, out[l])
+        res.append(out.cpu().numpy().copy())
+    return res
+
+
+def test_corrupted_plans_stay_exact():
+    w = _small(n_layers=3, layer_anchor=(0, 0, 0), steps=16, k=48, slots=64)
+    sel = _random_trace(w, seed=21)
+    for l in (1, 2):
+        sel[:, :, l] = sel[:, :, 0]
+    rng = np.random.default_rng(4)
+    R, k = w.n_requests, w.k
+    entry = 16 + 8 * k
+
+    def corrupt(t, l, plan):
+        buf = plan.cpu().numpy()
+        kind = (t + l) % 5
+        for i in range(R):
+            e = buf[16 + i * entry: 16 + (i + 1) * entry].view(np.int32)
+            m = int(e[0])
+            pos, slot = e[4: 4 + k], e[4 + k: 4 + 2 * k]
+            if kind == 0 and m > 1:
+                slot[:m] = np.roll(slot[:m], 1)
+            elif kind == 1:
+                e[0] = m // 2
+            elif kind == 2:
+                e[0] = k
+                pos[:] = rng.integers(0, w.n_positions, k)
+                slot[:] = rng.integers(0, w.slots, k)
+            elif kind == 3 and m > 0:
+                slot[0] = w.slots + 5          # invalid pair: flagged, never written
+        if kind == 4:
+            buf[12:16] = np.array([7], np.int32).view(np.uint8)   # wrong layer in header
+        plan.copy_(torch.from_numpy(buf))
+
+    with hs.Pool.for_workload(w) as pool:
+        fill_selected(pool, w, sel)
+        base = _run_group(pool, w, sel, None)
+        meta = {(r, l): (pool.views(l)["slot_pos"][r].cpu().numpy(),
+                         pool.views(l)["page_table"][r].cpu().numpy(),
+                         pool.views(l)["stamps"][r].cpu().numpy())
+                for r in range(R) for l in range(3)}
+        pool.reset()
+        st = pool.stats()
+        assert st["resolves"] == 0 and st["misses"] == 0
+        pre = _run_group(pool, w, sel, corrupt)
+        for a, b in zip(base, pre):
+            assert np.array_equal(a, b)
+        for (r, l), (sp, pt, stamps) in meta.items():
+            assert np.array_equal(pool.views(l)["slot_pos"][r].cpu().numpy(), sp)
+            assert np.array_equal(pool.views(l)["page_table"][r].cpu().numpy(), pt)
+            assert np.array_equal(pool.views(l)["stamps"][r].cpu().numpy(), stamps)
+            check_cache(pool, w, l, r, sp)
+        st = pool.stats(check=False)
+        assert st["plan_mismatches"] > 0 and st["status"] & hs.HS_STATUS_PLAN
+
+
+def test_cuda_graph_replay_matches_oracle():
+    w = configs.DSA_MLA.with_(n_requests=4, n_positions=20000, steps=20)
+    from workloads import traces
+    sel = traces.generate(w)
+    orc = _oracles(w)
+    with hs.Pool.for_workload(w) as pool:
+        fill_selected(pool, w, sel)
+        static_sel = torch.empty((w.n_layers, w.n_requests, w.k), dtype=torch.int32,
+                                 device="cuda")
+        out = torch.empty_like(static_sel)
+        dsel = torch.from_numpy(np.ascontiguousarray(sel.transpose(0, 2, 1, 3))).cuda()
+        s = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        static_sel.copy_(dsel[0])
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            for l in range(w.n_layers):
+                pool.resolve(l, static_sel[l], out[l], stream=s)
+        # capture records without running: the pool is still empty
+        assert pool.stats()["resolves"] == 0
+        for t in range(w.steps):
+            static_sel.copy_(dsel[t])
+            g.replay()
+            got = out.cpu().numpy()
+            for (r, l), p in orc.items():
+                rc, o, _ = p.resolve(sel[t, r, l], out_base=r * w.slots)
+                assert np.array_equal(got[l, r], o)
+        for (r, l), p in orc.items():
+            check_metadata(pool, w, l, r, p, w.steps)
+            check_cache(pool, w, l, r, p.slot_pos, sample=256)
+
+
+def test_link_probe_reports_bandwidth():
+    h2d, gather = hs.hs_link_probe(256 << 20, reps=3, record_bytes=1152)
+    assert h2d > 1.0 and gather > 1.0
+
+
+def test_host_records_layout():
+    w = _small()
+    with hs.Pool.for_workload(w) as pool:
+        a = pool.host_records(1, 1)
+        b = pool.host_records(2, 0)
+        assert a.shape == (w.n_positions, w.record_bytes)
+        gap = b.ctypes.data - a.ctypes.data
+        assert gap == w.n_positions * w.record_bytes   # host[r][l][pos][W]
+        a[:] = records.gen(w, 1, 1, np.arange(w.n_positions))
+        assert np.array_equal(pool.host_records(1, 1)[17], records.gen(w, 1, 1, [17])[0])

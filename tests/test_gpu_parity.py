@@ -1,0 +1,137 @@
+"""GPU path against the CPU oracle, bit for bit, on the five seeded workloads.
+
+Every step: the published slot of every selected entry of every
+(request, layer) and the per-layer miss count.  Periodically and at the last
+step: page table, slot map, stamps, LRU order and resolve count of every
+pair.  At the end: the bytes of every occupied slot (or a fixed sample for
+the largest workloads) against the host record of the position it holds,
+and the cumulative counters.  The launch configuration is the one the
+benchmark times (hs_resolve picks the cluster size from the request count).
+"""
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+import pytest
+import torch
+
+from hierarchical_kv_cache_resolve_gb300 import hs
+from tests.gpu_harness import (OracleRun, check_cache, check_metadata, device_trace,
+                               fill_selected)
+from workloads import configs, traces
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle_step(orc: OracleRun, sel_t, pool_ex):
+    items = list(orc.state.items())
+
+    def one(item):
+        (r, l), p = item
+        rc, out, m = p.resolve(sel_t[r, l], out_base=r * orc.w.slots)
+        assert rc == 0
+        return (r, l), (out, m)
+
+    return dict(pool_ex.map(one, items))
+
+
+def run_and_compare(w, meta_every=1, cache_sample=None, prefetch=False, sel=None):
+    if sel is None:
+        sel = traces.generate(w)
+    T, R, NL, k = sel.shape
+    orc = OracleRun(w)
+    ex = ThreadPoolExecutor(16)
+    with hs.Pool.for_workload(w) as pool:
+        fill_selected(pool, w, sel)
+        dsel = device_trace(sel)
+        out = torch.empty((NL, R, k), dtype=torch.int32, device="cuda")
+        main = torch.cuda.current_stream()
+        side = torch.cuda.Stream()
+        plans = {}
+        if prefetch:
+            nb = hs.hs_plan_bytes(R, k)
+            for l in range(NL):
+                if w.anchors[l] != l:
+                    plans[l] = torch.empty(nb, dtype=torch.uint8, device="cuda")
+        prev = {l: 0 for l in range(NL)}
+        for t in range(T):
+            for l in range(NL):
+                a = w.anchors[l]
+                if l in plans:
+                    pool.prefetch_plan(a, l, dsel[t, l], plans[l], stream=main)
+                    ev = torch.cuda.Event()
+                    ev.record(main)
+                    side.wait_event(ev)
+                    pool.prefetch_copy(l, R, k, plans[l], stream=side)
+                    ev2 = torch.cuda.Event()
+                    ev2.record(side)
+                    main.wait_event(ev2)
+                    pool.resolve(l, dsel[t, l], out[l], plan=plans[l], stream=main)
+                else:
+                    pool.resolve(l, dsel[t, l], out[l], stream=main)
+            ores = _oracle_step(orc, sel[t], ex)
+            got = out.cpu().numpy()
+            for (r, l), (o, m) in ores.items():
+                assert np.array_equal(got[l, r], o), (t, r, l)
+            for l in range(NL):
+                st = pool.stats(l)
+                misses = sum(ores[(r, l)][1] for r in range(R))
+                assert st["misses"] - prev[l] == misses, (t, l)
+                prev[l] = st["misses"]
+            if (t % meta_every == 0) or t == T - 1:
+                for (r, l), p in orc.state.items():
+                    check_metadata(pool, w, l, r, p, t + 1)
+        for (r, l), p in orc.state.items():
+            check_cache(pool, w, l, r, p.slot_pos, sample=cache_sample)
+        for l in range(NL):
+            st = pool.stats(l)
+            ps = [orc.state[(r, l)] for r in range(R)]
+            assert st["resolves"] == T * R
+            assert st["hits"] == sum(p.hits for p in ps)
+            assert st["misses"] == sum(p.misses for p in ps)
+            assert st["status"] == 0
+            if l in plans:
+                assert st["plan_mismatches"] == 0
+                assert st["plan_hits"] == st["misses"]
+                assert st["prefetched_bytes"] == st["misses"] * w.record_bytes
+                assert st["fetched_bytes"] == 0
+            else:
+                assert st["fetched_bytes"] == sum(p.fetched_bytes for p in ps)
+    ex.shutdown()
+    return orc
+
+
+def test_tiny_every_step():
+    run_and_compare(configs.TINY, meta_every=1)
+
+
+def test_tiny_with_ragged_request_set():
+    """Several requests with a k that is not a multiple of the warp size."""
+    w = configs.TINY.with_(n_requests=5, n_layers=2, k=45, slots=77, steps=40)
+    run_and_compare(w, meta_every=1)
+
+
+@pytest.mark.slow
+def test_dsa_mla_full():
+    run_and_compare(configs.DSA_MLA, meta_every=16)
+
+
+@pytest.mark.slow
+def test_no_locality_full():
+    run_and_compare(configs.NO_LOCALITY, meta_every=16)
+
+
+@pytest.mark.slow
+def test_quest_pages_full():
+    run_and_compare(configs.QUEST_PAGES, meta_every=32, cache_sample=512)
+
+
+@pytest.mark.slow
+def test_tight_prefetch_full_with_prefetch():
+    run_and_compare(configs.TIGHT_PREFETCH, meta_every=32, cache_sample=256, prefetch=True)
+
+
+def test_tight_prefetch_small_with_and_without_prefetch():
+    w = configs.TIGHT_PREFETCH.with_(n_requests=6, n_positions=20000, k=512, slots=512,
+                                     steps=24)
+    run_and_compare(w, meta_every=4, prefetch=False)
+    run_and_compare(w, meta_every=4, prefetch=True)

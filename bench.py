@@ -1,0 +1,487 @@
+"""Throughput of the RESOLVE step on one GB300 (or N, one process each).
+
+A step is one decode step of the whole hot path: every sparse layer's
+resolve (hash build, hit probe, victim choice, host fetch of the misses,
+metadata update, publication) for every request of the batch.  Default
+workload: the DSA/MLA-shaped trace -- 8 requests, 4 sparse layers,
+L_ctx = 131072, k = 2048, B = 4096, 1152-byte records (576 bf16) -- with
+its seeded 256-step selection trace (steps past the end wrap around).
+
+Passes, each on a freshly reset pool (warm-up steps first, then timed ones):
+  graph  -- each step is a CUDA graph of the per-layer hs_resolve launches;
+            the L2 is flushed (256 MiB write) before every step and the
+            step itself is timed with CUDA events: ``value``.
+  kernel -- the same steps launched one call at a time with events around
+            every launch: the average resolve-kernel duration (``roofline``).
+  e2e    -- the user's loop through the public API with host buffers:
+            pinned host -> device copy of the step's selections, the
+            resolves, device -> host copy of the published slots, a
+            synchronisation, all inside the timed region (``e2e``).
+The host-link ceiling is measured in the same run (pinned H2D memcpy and a
+scattered-record GPU-load probe, best of 10).  The CPU oracle is timed on
+the host's cores over a stated sample (``cpu_baseline``).
+
+``--impl reference`` times the CPU oracle alone as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = ("resolves/sec and miss-fetch GB/s (fraction of measured pinned H2D BW) "
+          "at 1 GB300")
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ---------------------------------------------------------------- helpers ---
+
+def workload_name(w) -> str:
+    return (f"{w.name}: batch {w.n_requests}, {w.n_layers} sparse layers, "
+            f"L_ctx={w.n_positions}, k={w.k}, B={w.slots}, W={w.record_bytes} B/record, "
+            f"{w.steps}-step seeded trace")
+
+
+def hbm_bytes_per_resolve(k: int, B: int, m: float, W: int) -> float:
+    """Algorithmic HBM bytes of one resolve with m misses (all victims
+    occupied, the steady state): reads selections 4k, slot map 4B, LRU order
+    2B; writes published slots 4k, stamps 4k (every selected slot), slot map
+    4m, page table 8m (new entry + evicted entry), LRU order 2B, records m*W."""
+    return 4 * k + 4 * B + 2 * B + 4 * k + 4 * k + 4 * m + 8 * m + 2 * B + m * W
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except OSError:
+        return None
+
+
+def reduce_max(value: float, dist_on: bool, device=None) -> float:
+    """Maximum of a float over all ranks (identity without torch.distributed)."""
+    if not dist_on:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(value: float, dist_on: bool, device=None) -> float:
+    if not dist_on:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def rank_workload(w, rank: int):
+    """Weak scaling: every rank owns its own batch of requests, with its own
+    seeded trace and records (seed offset by the rank)."""
+    return w.with_(seed=w.seed + rank)
+
+
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML (read-only)."""
+
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clock_setting"}
+
+    def __init__(self, pci_bus_id: str):
+        self.samples = []
+        self.max_mhz = None
+        self.err = None
+        self._stop = threading.Event()
+        self._thr = None
+        try:
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            self.h = ctypes.c_void_p()
+            if self.nvml.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(),
+                                                          ctypes.byref(self.h)) != 0:
+                raise OSError(f"no NVML handle for {pci_bus_id}")
+            mx = ctypes.c_uint()
+            if self.nvml.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+        except OSError as e:
+            self.err = str(e)
+            self.nvml = None
+
+    def _read(self):
+        clk = ctypes.c_uint()
+        rsn = ctypes.c_ulonglong()
+        self.nvml.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk))
+        self.nvml.nvmlDeviceGetCurrentClocksEventReasons(self.h, ctypes.byref(rsn))
+        return clk.value, rsn.value
+
+    def _run(self):
+        while not self._stop.is_set():
+            self.samples.append(self._read())
+            time.sleep(0.0005)
+
+    def start(self):
+        if self.nvml is not None:
+            self._thr = threading.Thread(target=self._run, daemon=True)
+            self._thr.start()
+
+    def stop(self):
+        self._stop.set()
+        if self._thr is not None:
+            self._thr.join()
+
+    def summary(self):
+        if self.nvml is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "source": f"unavailable: {self.err}"}
+        busy = [s for s in self.samples if not (s[1] & 0x1)] or self.samples
+        reasons = set()
+        for _, r in busy:
+            for bit, name in self.REASONS.items():
+                if r & bit and bit != 0x1:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median([c for c, _ in busy]) if busy else None,
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(reasons),
+                "samples": len(self.samples), "samples_not_idle": len(busy), "source": "nvml"}
+
+
+# ----------------------------------------------------------- CPU oracle ----
+
+def time_oracle(w, n_pairs: int, steps: int, threads: int):
+    """The CPU oracle as it stands, with host records and a cache mirror
+    (so it also copies every missed record), on the first n_pairs
+    (request, layer) pairs for `steps` steps of the trace, spread over
+    `threads` threads (one pair per task).  Returns (resolves/s, wall s,
+    resolves, miss bytes)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    from oracle.oracle import OK, Pair
+    from workloads import records, traces
+
+    pairs = [(r, l) for r in range(w.n_requests) for l in range(w.n_layers)][:n_pairs]
+    sel = traces.generate(w, requests=sorted({r for r, _ in pairs}))
+    rid = {r: i for i, r in enumerate(sorted({r for r, _ in pairs}))}
+    states = []
+    for r, l in pairs:
+        host = np.empty((w.n_positions, w.record_bytes), np.uint8)
+        records.fill(host.ctypes.data, w, r, l)
+        states.append(((r, l), Pair(w.slots, w.n_positions, w.record_bytes, host=host,
+                                    mirror=True)))
+    T = sel.shape[0]
+    idx = [s % T for s in range(steps)]
+
+    def run(item):
+        (r, l), p = item
+        ss = np.ascontiguousarray(sel[idx, rid[r], l, :])
+        rc, _, _ = p.run(ss, out_base=r * w.slots)
+        assert rc == OK
+        return p.fetched_bytes
+
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(threads) as ex:
+        fetched = sum(ex.map(run, states))
+    wall = time.perf_counter() - t0
+    n = len(pairs) * steps
+    return n / wall, wall, n, fetched
+
+
+def cpu_baseline(w, threads: int):
+    pairs = w.n_requests * w.n_layers
+    value, wall, n, fetched = time_oracle(w, pairs, w.steps, threads)
+    return {"value": value, "unit": "resolves/s", "cores": threads, "kind": "oracle",
+            "sample": (f"all {pairs} (request, layer) pairs x {w.steps} steps of the "
+                       f"{w.name} trace ({n} resolves, {fetched / 1e9:.2f} GB of misses "
+                       f"copied), one thread per pair, {threads} threads"),
+            "wall_s": wall, "miss_fetch_gbs": fetched / wall / 1e9}
+
+
+# -------------------------------------------------------------- GPU arm ----
+
+def run_gpu(args, w, rank, world, dist_on):
+    import torch
+
+    from hierarchical_kv_cache_resolve_gb300 import hs
+    from workloads import records, traces
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    props = torch.cuda.get_device_properties(dev)
+    pci = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+    R, NL, k, B, W, T = w.n_requests, w.n_layers, w.k, w.slots, w.record_bytes, w.steps
+
+    h2d_gbs, gather_gbs = hs.hs_link_probe(1 << 30, 10, W)
+
+    sel = traces.generate(w)
+    dsel = torch.from_numpy(np.ascontiguousarray(sel.transpose(0, 2, 1, 3))).to(dev)
+    pool = hs.Pool.for_workload(w)
+    for r in range(R):
+        for l in range(NL):
+            records.fill(pool.host_records(r, l).ctypes.data, w, r, l)
+    out = torch.empty((NL, R, k), dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    main = torch.cuda.current_stream()
+    Wm, K = args.warmup, args.steps
+    launches_per_step = NL * hs.hs_kernels_per_call()
+
+    def step_eager(t, stream=None):
+        for l in range(NL):
+            hs.hs_resolve(pool.handle, l, R, None, dsel[t, l], k, out[l], None, stream)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist_on:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # ---- graph pass -------------------------------------------------------
+    pool.reset()
+    cap = torch.cuda.Stream()
+    graphs = []
+    for t in range(T):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            for l in range(NL):
+                hs.hs_resolve(pool.handle, l, R, None, dsel[t, l], k, out[l], None, cap)
+        graphs.append(g)
+    for s in range(Wm):
+        flush.fill_(s)
+        graphs[s % T].replay()
+    st0 = pool.stats()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    sampler = ClockSampler(pci)
+    barrier()
+    sampler.start()
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.fill_(i)
+        ev[i][0].record(main)
+        graphs[(Wm + i) % T].replay()
+        ev[i][1].record(main)
+    barrier()
+    wall_graph = time.perf_counter() - wall0
+    sampler.stop()
+    st1 = pool.stats()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    dev_s = sum(step_ms) / 1e3
+    dev_s_max = reduce_max(dev_s, dist_on, dev)
+    fetched = st1["fetched_bytes"] - st0["fetched_bytes"]
+    misses = st1["misses"] - st0["misses"]
+    resolves = st1["resolves"] - st0["resolves"]
+    assert resolves == K * R * NL, (resolves, K * R * NL)
+    total_resolves = reduce_sum(resolves, dist_on, dev)
+    total_fetched = reduce_sum(fetched, dist_on, dev)
+    del graphs
+
+    # ---- kernel pass (per-launch events) ------------------------------------
+    pool.reset()
+    for s in range(Wm):
+        flush.fill_(s)
+        step_eager(s % T, main)
+    kst0 = pool.stats()
+    kev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(NL)] for _ in range(K)]
+    barrier()
+    for i in range(K):
+        flush.fill_(i)
+        t = (Wm + i) % T
+        for l in range(NL):
+            kev[i][l][0].record(main)
+            hs.hs_resolve(pool.handle, l, R, None, dsel[t, l], k, out[l], None, main)
+            kev[i][l][1].record(main)
+    barrier()
+    kst1 = pool.stats()
+    launch_ms = [a.elapsed_time(b) for row in kev for a, b in row]
+    avg_launch_s = sum(launch_ms) / len(launch_ms) / 1e3
+    k_launches = K * NL
+    k_fetched = kst1["fetched_bytes"] - kst0["fetched_bytes"]
+    k_misses = kst1["misses"] - kst0["misses"]
+    link_bytes_per_launch = k_fetched / k_launches
+    m_per_resolve = k_misses / (k_launches * R)
+    hbm_per_launch = R * hbm_bytes_per_resolve(k, B, m_per_resolve, W)
+
+    # ---- e2e pass (public API, host buffers) ----------------------------------
+    pool.reset()
+    host_sel = torch.from_numpy(np.ascontiguousarray(sel.transpose(0, 2, 1, 3))).pin_memory()
+    host_out = torch.empty((NL, R, k), dtype=torch.int32).pin_memory()
+    stage = torch.empty((NL, R, k), dtype=torch.int32, device=dev)
+
+    def e2e_step(t):
+        stage.copy_(host_sel[t], non_blocking=True)
+        for l in range(NL):
+            hs.hs_resolve(pool.handle, l, R, None, stage[l], k, out[l], None, main)
+        host_out.copy_(out, non_blocking=True)
+        main.synchronize()
+
+    for s in range(Wm):
+        e2e_step(s % T)
+    barrier()
+    e0 = time.perf_counter()
+    for i in range(K):
+        e2e_step((Wm + i) % T)
+    barrier()
+    e2e_s = reduce_max(time.perf_counter() - e0, dist_on, dev)
+    pool.close()
+
+    peaks = load_peaks()
+    hbm_peak = peaks.get("hbm_gbs") if peaks else None
+    miss_gbs = total_fetched / dev_s_max / 1e9
+    link_achieved = link_bytes_per_launch / avg_launch_s / 1e9
+    hbm_achieved = hbm_per_launch / avg_launch_s / 1e9
+    res = {
+        "metric": METRIC,
+        "value": total_resolves / dev_s_max,
+        "unit": "resolves/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": Wm,
+        "ms_per_step": dev_s_max / K * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int32",
+        "data": "synthetic",
+        "config": {
+            "workload": workload_name(w),
+            "global_batch": R * world,
+            "resolves_per_step": R * NL * world,
+            "parallelism": f"requests sharded, {world} independent pool(s), no collective",
+            "launch": f"per-step CUDA graph of {NL} hs_resolve launches",
+            "l2": "flushed before every timed step (256 MiB write, outside the events)",
+            "record_values": "bf16 N(0,1)" if w.value_format else "fp16 U(-1,1)",
+        },
+        "miss_fetch": {
+            "gbs": miss_gbs,
+            "unit": "GB/s",
+            "over": "device time of the timed steps",
+            "bytes": total_fetched,
+            "misses": misses,
+            "miss_rate": misses / (resolves * k),
+            "link_h2d_ceiling_gbs": h2d_gbs,
+            "frac_of_h2d": miss_gbs / h2d_gbs,
+            "in_kernel_gbs": link_achieved,
+            "in_kernel_frac_of_h2d": link_achieved / h2d_gbs,
+            "gather_probe_gbs": gather_gbs,
+        },
+        "roofline": {
+            "kernel": "resolve_kernel",
+            "bound": "link",
+            "achieved": link_achieved,
+            "peak": h2d_gbs,
+            "unit": "GB/s",
+            "frac": link_achieved / h2d_gbs,
+            "traffic": None,
+            "peak_source": "pinned cudaMemcpyAsync H2D, 1 GiB, best of 10, this run",
+            "algorithmic_bytes_per_launch": link_bytes_per_launch,
+            "avg_launch_us": avg_launch_s * 1e6,
+        },
+        "roofline_hbm": {
+            "kernel": "resolve_kernel",
+            "bound": "hbm",
+            "achieved": hbm_achieved,
+            "peak": hbm_peak,
+            "unit": "GB/s",
+            "frac": (hbm_achieved / hbm_peak) if hbm_peak else None,
+            "traffic": None,
+            "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if hbm_peak else None,
+            "algorithmic_bytes_per_launch": hbm_per_launch,
+        },
+        "e2e": {
+            "value": total_resolves / e2e_s,
+            "unit": "resolves/s",
+            "h2d_bytes_per_step": NL * R * k * 4,
+            "d2h_bytes_per_step": NL * R * k * 4,
+            "what": "pinned H2D of the step's selections, hs_resolve per layer, D2H of the "
+                    "published slots, stream synchronize; wall clock",
+        },
+        "gpu_launches": K * launches_per_step,
+        "clocks": sampler.summary(),
+        "graph_wall_s": wall_graph,
+    }
+    return res
+
+
+# ------------------------------------------------------------------ main ----
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1024)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="dsa_mla")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-threads", type=int, default=0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    from workloads import configs
+    base = configs.BY_NAME[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    threads = args.cpu_threads or len(os.sched_getaffinity(0))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        w = base
+        value, wall, n, fetched = time_oracle(w, w.n_requests * w.n_layers,
+                                              args.warmup + args.steps, threads)
+        res = {"impl": "reference", "metric": METRIC, "value": value, "unit": "resolves/s",
+               "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+               "ms_per_step": wall / (args.warmup + args.steps) * 1e3,
+               "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+               "dtype": "int32", "data": "synthetic",
+               "config": {"workload": workload_name(w), "global_batch": w.n_requests},
+               "cpu_baseline": {"value": value, "unit": "resolves/s", "cores": threads,
+                                "kind": "oracle",
+                                "sample": (f"the CPU oracle on all {w.n_requests * w.n_layers} "
+                                           f"(request, layer) pairs x "
+                                           f"{args.warmup + args.steps} steps, one thread per "
+                                           f"pair, {threads} threads; warm-up included")},
+               "e2e": {"value": value, "unit": "resolves/s", "h2d_bytes_per_step": 0,
+                       "d2h_bytes_per_step": 0},
+               "miss_fetch": {"gbs": fetched / wall / 1e9, "unit": "GB/s"}}
+        print(json.dumps(res))
+        return 0
+
+    import torch
+    dist_on = world > 1
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the resolve path has no CPU fallback)")
+    torch.cuda.set_device(local)
+    if dist_on:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    w = rank_workload(base, rank)
+    res = run_gpu(args, w, rank, world, dist_on)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(base, threads)
+        print(json.dumps(res))
+    if dist_on:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

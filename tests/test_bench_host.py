@@ -1,0 +1,84 @@
+"""Host-side logic of bench.py: byte accounting, weak-scaling reductions over
+ranks (gloo, world size 2, on CPU) and the reference arm's JSON line."""
+import json
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+from workloads import configs
+
+
+def test_hbm_bytes_per_resolve_by_hand():
+    k, B, m, W = 2048, 4096, 267, 1152
+    reads = 4 * k + 4 * B + 2 * B            # selections, slot map, LRU order
+    writes = 4 * k + 4 * k + 4 * m + 8 * m + 2 * B + m * W
+    assert bench.hbm_bytes_per_resolve(k, B, m, W) == reads + writes
+
+
+def test_rank_workloads_differ_only_in_seed():
+    a, b = bench.rank_workload(configs.DSA_MLA, 0), bench.rank_workload(configs.DSA_MLA, 1)
+    assert a.seed != b.seed
+    assert a.with_(seed=0) == b.with_(seed=0) == configs.DSA_MLA
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    t = bench.reduce_max(1.5 + rank, True)      # per-rank time
+    n = bench.reduce_sum(100.0 * (rank + 1), True)   # per-rank resolves
+    dist.barrier()
+    if rank == 0:
+        q.put((t, n, n / t))
+    dist.destroy_process_group()
+
+
+def test_weak_scaling_reduction_two_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    mp.start_processes(_worker, args=(2, port, q), nprocs=2, join=True, start_method="spawn")
+    t, n, v = q.get(timeout=30)
+    assert t == 2.5          # the slowest rank's time
+    assert n == 300.0        # all ranks' resolves
+    assert v == pytest.approx(120.0)
+
+
+def test_single_rank_reductions_are_identity():
+    assert bench.reduce_max(3.0, False) == 3.0
+    assert bench.reduce_sum(3.0, False) == 3.0
+
+
+def test_reference_arm_json(capsys):
+    rc = bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "5",
+                     "--warmup", "3", "--cpu-threads", "2"])
+    assert rc == 0
+    line = capsys.readouterr().out.strip().splitlines()[-1]
+    d = json.loads(line)
+    assert d["impl"] == "reference" and d["unit"] == "resolves/s" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 2
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["higher_is_better"] is True
+
+
+def test_warmup_floor():
+    with pytest.raises(SystemExit):
+        bench.main(["--impl", "reference", "--warmup", "2"])
+
+
+def test_gpu_arm_refuses_without_cuda():
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(SystemExit):
+        bench.main(["--steps", "3", "--warmup", "3"])

@@ -123,6 +123,8 @@ enum Hdr : int {
     H_NF = 6,        // atomic fill counter of the plan-mode fetch list
     H_PMISS = 7,     // plan-mode mismatches
     H_PHIT = 8,      // plan-mode plan hits
+    H_G = 9,         // follower: predicted misses in its share
+    H_NX = 10,       // follower: leader misses it did not predict
     H_SUMS = 16,     // kWarps scan sums from here
 };
 

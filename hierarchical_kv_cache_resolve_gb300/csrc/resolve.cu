@@ -3,8 +3,9 @@
 // Launch"; Pith review of arXiv 2608.07009, "What carries the argument").
 //
 // Grid: one thread-block cluster per request (n_req * C CTAs of kThreads).
+//
 // CTA 0 of a cluster (the leader) owns the request's metadata:
-//   P0  load the k selections, the slot map and the LRU order into shared
+//   P0  cp.async the k selections, the slot map and the LRU order into shared
 //       memory; reject positions outside [0, L) and corrupt metadata;
 //   P1  insert the selections into a shared-memory open-addressing hash
 //       table (key = position, value = selection index); a repeated key is
@@ -16,11 +17,20 @@
 //       order): the j-th miss gets the j-th non-hit slot as its victim;
 //   P4  publish slots, update page table / slot map / stamps, and rebuild
 //       the LRU order with a second ballot scan over the slots.
-// After P3 the fetch list (position, victim) is in the leader's shared
-// memory; the other CTAs of the cluster copy it through distributed shared
-// memory and fetch the records from the mapped host pool with 16-byte
-// non-coherent loads, while the leader commits the metadata.  With a
-// cluster of one CTA the leader fetches too.
+//
+// CTAs 1..C-1 (the followers) move the data.  Follower f owns a contiguous
+// share of the selection indices.  Before the leader has decided anything it
+// predicts which of its selections miss from the page table (a position
+// with no slot is a miss), compacts them and issues the 16-byte
+// non-coherent loads of those host records into registers, so that the
+// host-link transfer overlaps the leader's P0-P3.  After the cluster barrier
+// it reads the leader's verdict through distributed shared memory: every
+// predicted miss gets its victim slot (or is dropped if the leader found a
+// hit), and any miss of its share it did not predict is fetched as well, so
+// the leader's decision is always the one applied.  The leader commits the
+// metadata (P4) while the followers store.  A cluster of one CTA does all
+// of it in the leader, fetch after P3.  A resolve that consumes a prefetch
+// plan uses the leader's fetch list instead of the prediction.
 //
 // Victim selection without sorting: the LRU order array is kept sorted by
 // (stamp, slot).  A resolve at step t keeps the untouched slots in their old
@@ -61,6 +71,12 @@ __device__ __forceinline__ void cluster_arrive() {
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
 
+// Arrival that publishes nothing: it does not wait for this thread's
+// outstanding memory operations (a follower's in-flight host loads).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -69,10 +85,48 @@ __device__ __forceinline__ void cluster_wait() {
 // host pool, which no kernel writes.
 __device__ __forceinline__ uint4 ld_nc_v4(const void *p) {
     uint4 v;
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-        : "l"(p));
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
     return v;
+}
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *g) {
+    const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(g) : "memory");
+}
+
+__device__ __forceinline__ void cp_async4(void *smem, const void *g) {
+    const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(s), "l"(g) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// Issues an asynchronous global -> shared copy of nbytes (by the whole CTA):
+// 16-byte pieces while both sides are 16-byte aligned, 4-byte pieces after
+// that, plain 2-byte loads for what is left.  Completed by cp_async_wait_all
+// and a barrier.
+__device__ __forceinline__ void copy_to_smem(void *dst, const void *src, int nbytes) {
+    uint8_t *d = static_cast<uint8_t *>(dst);
+    const uint8_t *s = static_cast<const uint8_t *>(src);
+    int done = 0;
+    if (((reinterpret_cast<uintptr_t>(d) | reinterpret_cast<uintptr_t>(s)) & 15u) == 0) {
+        const int n16 = nbytes >> 4;
+        for (int i = threadIdx.x; i < n16; i += kThreads) cp_async16(d + 16 * i, s + 16 * i);
+        done = n16 << 4;
+    }
+    if (((reinterpret_cast<uintptr_t>(d + done) | reinterpret_cast<uintptr_t>(s + done)) & 3u) == 0) {
+        const int n4 = (nbytes - done) >> 2;
+        for (int i = threadIdx.x; i < n4; i += kThreads)
+            cp_async4(d + done + 4 * i, s + done + 4 * i);
+        done += n4 << 2;
+    }
+    // what is left is made of 2-byte elements (u16 arrays of odd length)
+    for (int i = done / 2 + threadIdx.x; i < nbytes / 2; i += kThreads)
+        reinterpret_cast<uint16_t *>(d)[i] = reinterpret_cast<const uint16_t *>(s)[i];
 }
 
 __device__ __forceinline__ uint32_t hash_pos(int32_t pos, int H) {
@@ -80,15 +134,16 @@ __device__ __forceinline__ uint32_t hash_pos(int32_t pos, int H) {
 }
 
 // Copies F records: fetch-list entry j moves host_pair[fp[j]] to
-// cache_pair[fs[j]].  The 16-byte chunks (entry, part) are spread over G
-// threads; each thread keeps kUnroll loads in flight before storing.
+// cache_pair[fs[j]] (entries with fs[j] < 0 are skipped).  The 16-byte
+// chunks (entry, part) are spread over G threads; each thread keeps kUnroll
+// loads in flight before storing.  `q_begin` skips chunks already done.
 __device__ __forceinline__ void fetch_records(const uint8_t *__restrict__ host_pair,
                                               uint8_t *__restrict__ cache_pair,
                                               const int32_t *fp, const int32_t *fs, int F,
-                                              int W, int g, int G) {
+                                              int W, int g, int G, int q_begin = 0) {
     const int CW = W >> 4;
     const int Q = F * CW;
-    for (int q0 = g; q0 < Q; q0 += G * kUnroll) {
+    for (int q0 = q_begin + g; q0 < Q; q0 += G * kUnroll) {
         uint4 v[kUnroll];
         int64_t doff[kUnroll];
 #pragma unroll
@@ -98,8 +153,11 @@ __device__ __forceinline__ void fetch_records(const uint8_t *__restrict__ host_p
             if (q < Q) {
                 const int j = q / CW;
                 const int part = q - j * CW;
-                v[u] = ld_nc_v4(host_pair + (int64_t)fp[j] * W + part * 16);
-                doff[u] = (int64_t)fs[j] * W + part * 16;
+                const int32_t slot = fs[j];
+                if (slot >= 0) {
+                    v[u] = ld_nc_v4(host_pair + (int64_t)fp[j] * W + part * 16);
+                    doff[u] = (int64_t)slot * W + part * 16;
+                }
             }
         }
 #pragma unroll
@@ -134,7 +192,7 @@ __device__ __forceinline__ uint32_t warp_counts_exscan(uint32_t mine, uint32_t *
 }
 
 template <bool kPlanOnly>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 1)
     resolve_kernel(DevPool p, int layer, int n_req, const int32_t *__restrict__ req_ids,
                    const int32_t *__restrict__ sel_g, int k, int32_t *__restrict__ out_g,
                    const uint8_t *__restrict__ plan_in, uint8_t *__restrict__ plan_out) {
@@ -160,49 +218,64 @@ __global__ void __launch_bounds__(kThreads)
     const uint32_t crank = kPlanOnly ? 0u : cluster_ctarank();
     const uint32_t csize = kPlanOnly ? 1u : cluster_nctarank();
     const int ireq = (int)(blockIdx.x / csize);
-    const int B = p.B, H = sl.H;
+    const int B = p.B, H = sl.H, W = p.W;
+    const int32_t *selr = sel_g + (int64_t)ireq * k;
+
+    if (tid < H_SUMS) hdr[tid] = 0u;
+    if (crank == 0) copy_to_smem(sel_s, selr, 4 * k);  // independent of the request id
+
     const int r = req_ids ? req_ids[ireq] : ireq;
     const bool r_ok = r >= 0 && r < p.R;
     const int64_t pair = (int64_t)layer * p.R + (r_ok ? r : 0);
+    const uint8_t *host_pair = p.host + ((int64_t)(r_ok ? r : 0) * p.NL + layer) * p.L * W;
+    uint8_t *cache_pair = p.cache + pair * B * (int64_t)W;
+
+    // follower state (registers): predicted misses and their preloaded chunks
+    uint4 pre[kUnroll];
+    int npre = 0;
 
     if (crank == 0) {
         // ---------------- P0: load -------------------------------------
-        if (tid < H_SUMS) hdr[tid] = 0u;
-        __syncthreads();
         bool took_busy = false;
+        if (r_ok) {
+            copy_to_smem(spos_s, p.slot_pos + pair * B, 4 * B);
+            copy_to_smem(order_s, p.lru + pair * B, 2 * B);
+        }
+        for (int h = tid; h < H; h += kThreads) tab[h] = 0ull;
+        uint32_t a0 = 0, t0 = 0;
         if (tid == 0) {
-            uint32_t a = 0;
             if (!r_ok) {
-                a |= HS_STATUS_REQ_RANGE;
+                a0 |= HS_STATUS_REQ_RANGE;
             } else if (!kPlanOnly) {
                 if (atomicCAS(&p.busy[pair], 0u, 1u) == 0u)
                     took_busy = true;
                 else
-                    a |= HS_STATUS_REQ_BUSY;
+                    a0 |= HS_STATUS_REQ_BUSY;
             }
-            if (a) atomicOr(&hdr[H_ABORT], a);
-            hdr[H_T] = r_ok ? p.tcount[pair] + 1u : 0u;
+            t0 = r_ok ? p.tcount[pair] + 1u : 0u;
         }
-        if (r_ok) {
-            const int32_t *selr = sel_g + (int64_t)ireq * k;
+        cp_async_wait_all();
+        __syncthreads();  // header zeroed, shared copies landed
+        {
+            uint32_t bad = 0;
+            if (tid == 0) {
+                bad = a0;
+                hdr[H_T] = t0;
+            }
             for (int i = tid; i < k; i += kThreads) {
-                const int32_t v = selr[i];
-                sel_s[i] = v;
+                const int32_t v = sel_s[i];
                 hit_s[i] = -1;
-                if (v < 0 || (int64_t)v >= p.L) atomicOr(&hdr[H_ABORT], HS_STATUS_POS_RANGE);
+                if (v < 0 || (int64_t)v >= p.L) bad |= HS_STATUS_POS_RANGE;
             }
-            const int32_t *sp = p.slot_pos + pair * B;
-            const uint16_t *lo = p.lru + pair * B;
-            for (int b = tid; b < B; b += kThreads) {
-                const int32_t v = sp[b];
-                const uint16_t o = lo[b];
-                spos_s[b] = v;
-                order_s[b] = o;
-                flags_s[b] = 0;
-                if (v < -1 || (int64_t)v >= p.L || o >= (uint16_t)B)
-                    atomicOr(&hdr[H_ABORT], HS_STATUS_META);
+            if (r_ok) {
+                for (int b = tid; b < B; b += kThreads) {
+                    const int32_t v = spos_s[b];
+                    flags_s[b] = 0;
+                    if (v < -1 || (int64_t)v >= p.L || order_s[b] >= (uint16_t)B)
+                        bad |= HS_STATUS_META;
+                }
             }
-            for (int h = tid; h < H; h += kThreads) tab[h] = 0ull;
+            if (bad) atomicOr(&hdr[H_ABORT], bad);
         }
         __syncthreads();
 
@@ -384,23 +457,162 @@ __global__ void __launch_bounds__(kThreads)
             }
             return;
         }
+    } else if (!with_plan) {
+        // ---------------- follower F0-F2: predict misses, start the loads --
+        const int nf = csize > 1 ? (int)csize - 1 : 1, f = (int)crank - 1;
+        const int i0 = (int)((int64_t)f * k / nf), i1 = (int)((int64_t)(f + 1) * k / nf);
+        const int ns = i1 - i0;
+        int32_t *gi = hit_s;     // predicted misses: selection index
+        int32_t *gp = mpos;      //                   position
+        uint8_t *gbit = flags_s; // prediction per share entry
+        copy_to_smem(sel_s, selr + i0, 4 * ns);
+        cp_async_wait_all();
+        __syncthreads();
+        const int32_t *pt = p.pt + pair * p.L;
+        const int seg = (ns + kThreads - 1) / kThreads;
+        const int base_e = warp * 32 * seg;
+        uint32_t cnt = 0;
+        for (int s0 = 0; s0 < seg; s0 += 8) {
+            int32_t ptv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int e = base_e + (s0 + u) * 32 + lane;
+                ptv[u] = 0;
+                if (s0 + u < seg && e < ns && r_ok) {
+                    const int32_t pos = sel_s[e];
+                    if (pos >= 0 && (int64_t)pos < p.L) ptv[u] = pt[pos];
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (s0 + u >= seg) break;
+                const int e = base_e + (s0 + u) * 32 + lane;
+                const bool g = e < ns && ptv[u] == -1;
+                if (e < ns) gbit[e] = g ? 1 : 0;
+                cnt += __popc(__ballot_sync(0xFFFFFFFFu, g));
+            }
+        }
+        uint32_t total;
+        uint32_t rank = warp_counts_exscan(cnt, sums, &total);
+        const uint32_t lt = lanemask_lt();
+        for (int s = 0; s < seg; ++s) {
+            const int e = base_e + s * 32 + lane;
+            const bool g = e < ns && gbit[e];
+            const uint32_t bal = __ballot_sync(0xFFFFFFFFu, g);
+            if (g) {
+                const uint32_t j = rank + __popc(bal & lt);
+                gi[j] = i0 + e;
+                gp[j] = sel_s[e];
+            }
+            rank += __popc(bal);
+        }
+        if (tid == 0) hdr[H_G] = total;
+        __syncthreads();
+        const int CW = W >> 4;
+        const int Q = (int)total * CW;
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int q = tid + u * kThreads;
+            if (q < Q) {
+                const int j = q / CW;
+                pre[u] = ld_nc_v4(host_pair + (int64_t)gp[j] * W + (q - j * CW) * 16);
+                npre = u + 1;
+            }
+        }
     }
 
     if constexpr (!kPlanOnly) {
-        // ---------------- hand the fetch list to the cluster --------------
-        cluster_arrive();  // phase A: leader has published
+        // phase A: the leader publishes its decision (release); a follower
+        // only says it is ready, without waiting for its loads in flight
+        if (crank == 0)
+            cluster_arrive();
+        else
+            cluster_arrive_relaxed();
         cluster_wait();
-        const int32_t *fp = mpos, *fs = mslot;
-        int F = 0;
+
         if (crank == 0) {
-            F = (int)hdr[H_F];
-            if (hdr[H_FLIST]) { fp = fpos; fs = fslot; }
-        } else {
-            // copy the leader's list into the same place of this CTA's
-            // shared memory (the layouts are identical)
+            cluster_arrive_relaxed();  // phase B: the leader's shared memory stays valid until B
+            if (hdr[H_ABORT] == 0u) {
+                // ------------- P4: commit metadata, publish ------------------
+                const uint32_t t = hdr[H_T];
+                const int m = (int)hdr[H_M];
+                const int nh = (int)hdr[H_NH];
+                int32_t *o = out_g + (int64_t)ireq * k;
+                const int32_t rowbase = r * B;
+                for (int i = tid; i < k; i += kThreads) {
+                    const int32_t hsl = hit_s[i];
+                    o[i] = rowbase + (hsl >= 0 ? hsl : mslot[-2 - hsl]);
+                }
+                int32_t *pt = p.pt + pair * p.L;
+                int32_t *sp = p.slot_pos + pair * B;
+                uint32_t *st = p.stamp + pair * B;
+                for (int j = tid; j < m; j += kThreads) {
+                    const int32_t v = mslot[j];
+                    const int32_t old = spos_s[v];
+                    if (old >= 0) pt[old] = -1;
+                    pt[mpos[j]] = v;
+                    sp[v] = mpos[j];
+                    st[v] = 2u * t - 1u;
+                }
+                // new LRU order: [untouched (placed by P3)] [victims] [hits]
+                const int segB = (B + kThreads - 1) / kThreads;
+                const int baseB = warp * 32 * segB;
+                const uint32_t lt = lanemask_lt();
+                uint32_t cv = 0, ch = 0;
+                for (int s = 0; s < segB; ++s) {
+                    const int b = baseB + s * 32 + lane;
+                    const uint8_t fl = b < B ? flags_s[b] : 0;
+                    cv += __popc(__ballot_sync(0xFFFFFFFFu, (fl & 2) != 0));
+                    ch += __popc(__ballot_sync(0xFFFFFFFFu, (fl & 1) != 0));
+                }
+                uint32_t total;
+                const uint32_t base = warp_counts_exscan(cv | (ch << 16), sums, &total);
+                uint32_t vr = (uint32_t)(nh - m) + (base & 0xFFFFu);
+                uint32_t hr = (uint32_t)nh + (base >> 16);
+                for (int s = 0; s < segB; ++s) {
+                    const int b = baseB + s * 32 + lane;
+                    const uint8_t fl = b < B ? flags_s[b] : 0;
+                    const uint32_t bv = __ballot_sync(0xFFFFFFFFu, (fl & 2) != 0);
+                    const uint32_t bh = __ballot_sync(0xFFFFFFFFu, (fl & 1) != 0);
+                    if (fl & 2) neworder[vr + __popc(bv & lt)] = (uint16_t)b;
+                    if (fl & 1) {
+                        neworder[hr + __popc(bh & lt)] = (uint16_t)b;
+                        st[b] = 2u * t;
+                    }
+                    vr += __popc(bv);
+                    hr += __popc(bh);
+                }
+                __syncthreads();
+                uint16_t *lo = p.lru + pair * B;
+                for (int b = tid; b < B; b += kThreads) lo[b] = neworder[b];
+                const int F = (int)hdr[H_F];
+                if (tid == 0) {
+                    p.tcount[pair] = t;
+                    unsigned long long *c = p.counters + (int64_t)layer * CTR_COUNT;
+                    atomicAdd(&c[CTR_RESOLVES], 1ull);
+                    atomicAdd(&c[CTR_HITS], (unsigned long long)(k - m));
+                    atomicAdd(&c[CTR_MISSES], (unsigned long long)m);
+                    atomicAdd(&c[CTR_FETCHED], (unsigned long long)F * (unsigned long long)W);
+                    if (with_plan) {
+                        atomicAdd(&c[CTR_PLAN_HITS], (unsigned long long)hdr[H_PHIT]);
+                        atomicAdd(&c[CTR_PLAN_MISMATCH], (unsigned long long)hdr[H_PMISS]);
+                    }
+                }
+                if (csize == 1 && F > 0) {
+                    const bool plist = hdr[H_FLIST] != 0u;
+                    fetch_records(host_pair, cache_pair, plist ? fpos : mpos,
+                                  plist ? fslot : mslot, F, W, tid, kThreads);
+                }
+                if (tid == 0) {
+                    __threadfence();
+                    atomicExch(&p.busy[pair], 0u);
+                }
+            }
+        } else if (with_plan) {
+            // ------------- follower, plan consumed: the leader's fetch list ----
             cg::cluster_group cl = cg::this_cluster();
             const uint32_t *lh = cl.map_shared_rank(hdr, 0);
-            F = (int)lh[H_F];
+            const int F = (int)lh[H_F];
             const bool plist = lh[H_FLIST] != 0u;
             int32_t *dp = plist ? fpos : mpos;
             int32_t *ds = plist ? fslot : mslot;
@@ -410,95 +622,65 @@ __global__ void __launch_bounds__(kThreads)
                 dp[e] = lp[e];
                 ds[e] = ls[e];
             }
-            fp = dp;
-            fs = ds;
             __syncthreads();
-        }
-        cluster_arrive();  // phase B: the leader's fetch list may be released
-
-        const uint8_t *host_pair = p.host + ((int64_t)(r_ok ? r : 0) * p.NL + layer) * p.L * p.W;
-        uint8_t *cache_pair = p.cache + pair * B * p.W;
-
-        if (crank == 0 && hdr[H_ABORT] == 0u) {
-            // ------------- P4: commit metadata, publish ------------------
-            const uint32_t t = hdr[H_T];
-            const int m = (int)hdr[H_M];
-            const int nh = (int)hdr[H_NH];
-            int32_t *o = out_g + (int64_t)ireq * k;
-            const int32_t rowbase = r * B;
-            for (int i = tid; i < k; i += kThreads) {
-                const int32_t hsl = hit_s[i];
-                o[i] = rowbase + (hsl >= 0 ? hsl : mslot[-2 - hsl]);
-            }
-            int32_t *pt = p.pt + pair * p.L;
-            int32_t *sp = p.slot_pos + pair * B;
-            uint32_t *st = p.stamp + pair * B;
-            for (int j = tid; j < m; j += kThreads) {
-                const int32_t v = mslot[j];
-                const int32_t old = spos_s[v];
-                if (old >= 0) pt[old] = -1;
-                pt[mpos[j]] = v;
-                sp[v] = mpos[j];
-                st[v] = 2u * t - 1u;
-            }
-            // new LRU order: [untouched (already placed by P3)] [victims] [hits]
-            const int segB = (B + kThreads - 1) / kThreads;
-            const int baseB = warp * 32 * segB;
-            const uint32_t lt = lanemask_lt();
-            uint32_t cv = 0, ch = 0;
-            for (int s = 0; s < segB; ++s) {
-                const int b = baseB + s * 32 + lane;
-                const uint8_t f = b < B ? flags_s[b] : 0;
-                cv += __popc(__ballot_sync(0xFFFFFFFFu, (f & 2) != 0));
-                ch += __popc(__ballot_sync(0xFFFFFFFFu, (f & 1) != 0));
-            }
-            uint32_t total;
-            const uint32_t base = warp_counts_exscan(cv | (ch << 16), sums, &total);
-            uint32_t vr = (uint32_t)(nh - m) + (base & 0xFFFFu);
-            uint32_t hr = (uint32_t)nh + (base >> 16);
-            for (int s = 0; s < segB; ++s) {
-                const int b = baseB + s * 32 + lane;
-                const uint8_t f = b < B ? flags_s[b] : 0;
-                const uint32_t bv = __ballot_sync(0xFFFFFFFFu, (f & 2) != 0);
-                const uint32_t bh = __ballot_sync(0xFFFFFFFFu, (f & 1) != 0);
-                if (f & 2) neworder[vr + __popc(bv & lt)] = (uint16_t)b;
-                if (f & 1) {
-                    neworder[hr + __popc(bh & lt)] = (uint16_t)b;
-                    st[b] = 2u * t;
+            cluster_arrive_relaxed();  // phase B: done reading the leader
+            if (F > 0)
+                fetch_records(host_pair, cache_pair, dp, ds, F, W, (int)(crank - 1) * kThreads + tid,
+                              (int)(csize - 1) * kThreads);
+        } else {
+            // ------------- follower F3-F6: apply the leader's verdict ----------
+            cg::cluster_group cl = cg::this_cluster();
+            const uint32_t *lh = cl.map_shared_rank(hdr, 0);
+            const int32_t *lhit = cl.map_shared_rank(hit_s, 0);
+            const int32_t *lmslot = cl.map_shared_rank(mslot, 0);
+            const bool abort = lh[H_ABORT] != 0u;
+            const int nf = csize > 1 ? (int)csize - 1 : 1, f = (int)crank - 1;
+            const int i0 = (int)((int64_t)f * k / nf), i1 = (int)((int64_t)(f + 1) * k / nf);
+            const int ns = i1 - i0;
+            const int g = (int)hdr[H_G];
+            int32_t *gi = hit_s;
+            int32_t *gp = mpos;
+            int32_t *gs = mslot;           // victim slot of each predicted miss, -1 = drop
+            uint8_t *gbit = flags_s;
+            int32_t *xp = spos_s;          // leader misses that were not predicted
+            int32_t *xs = reinterpret_cast<int32_t *>(tab);
+            if (!abort) {
+                for (int j = tid; j < g; j += kThreads) {
+                    const int32_t hsl = lhit[gi[j]];
+                    gs[j] = hsl <= -2 ? lmslot[-2 - hsl] : -1;
                 }
-                vr += __popc(bv);
-                hr += __popc(bh);
-            }
-            __syncthreads();
-            uint16_t *lo = p.lru + pair * B;
-            for (int b = tid; b < B; b += kThreads) lo[b] = neworder[b];
-            if (tid == 0) {
-                p.tcount[pair] = t;
-                unsigned long long *c = p.counters + (int64_t)layer * CTR_COUNT;
-                atomicAdd(&c[CTR_RESOLVES], 1ull);
-                atomicAdd(&c[CTR_HITS], (unsigned long long)(k - m));
-                atomicAdd(&c[CTR_MISSES], (unsigned long long)m);
-                atomicAdd(&c[CTR_FETCHED], (unsigned long long)F * (unsigned long long)p.W);
-                if (with_plan) {
-                    atomicAdd(&c[CTR_PLAN_HITS], (unsigned long long)hdr[H_PHIT]);
-                    atomicAdd(&c[CTR_PLAN_MISMATCH], (unsigned long long)hdr[H_PMISS]);
+                for (int e = tid; e < ns; e += kThreads) {
+                    const int32_t hsl = lhit[i0 + e];
+                    if (hsl <= -2 && !gbit[e]) {
+                        const uint32_t x = atomicAdd(&hdr[H_NX], 1u);
+                        xp[x] = sel_s[e];
+                        xs[x] = lmslot[-2 - hsl];
+                    }
                 }
             }
+            __syncthreads();
+            cluster_arrive_relaxed();  // phase B: done reading the leader
+            if (!abort) {
+                const int CW = W >> 4;
+                const int Q = g * CW;
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    const int q = tid + u * kThreads;
+                    if (u < npre && q < Q) {
+                        const int j = q / CW;
+                        const int32_t slot = gs[j];
+                        if (slot >= 0)
+                            *reinterpret_cast<uint4 *>(cache_pair + (int64_t)slot * W +
+                                                       (q - j * CW) * 16) = pre[u];
+                    }
+                }
+                fetch_records(host_pair, cache_pair, gp, gs, g, W, tid, kThreads,
+                              kUnroll * kThreads);
+                const int nx = (int)hdr[H_NX];
+                if (nx > 0) fetch_records(host_pair, cache_pair, xp, xs, nx, W, tid, kThreads);
+            }
         }
-
-        // ---------------- P5: fetch the records -----------------------------
-        if (F > 0) {
-            if (csize == 1)
-                fetch_records(host_pair, cache_pair, fp, fs, F, p.W, tid, kThreads);
-            else if (crank > 0)
-                fetch_records(host_pair, cache_pair, fp, fs, F, p.W,
-                              (int)(crank - 1) * kThreads + tid, (int)(csize - 1) * kThreads);
-        }
-        if (crank == 0 && tid == 0 && hdr[H_ABORT] == 0u) {
-            __threadfence();
-            atomicExch(&p.busy[pair], 0u);
-        }
-        cluster_wait();  // phase B: no CTA leaves while the leader's list is read
+        cluster_wait();  // phase B: no CTA leaves while the leader is being read
     }
 }
 

@@ -142,6 +142,37 @@ def test_shapes(shape):
                 for l in range(w.n_layers))
 
 
+@pytest.mark.parametrize("cluster", ["1", "2", "4", "8"])
+def test_every_cluster_size(cluster, monkeypatch):
+    """Leader-only (1 CTA) and 1, 3, 7 followers give the same result."""
+    monkeypatch.setenv("HS_CLUSTER", cluster)
+    w = _small(n_requests=4, k=300, slots=512, n_positions=5000, steps=12)
+    sel = _random_trace(w, seed=17)
+    # give consecutive steps some overlap so that hits, misses and evictions mix
+    for t in range(1, w.steps):
+        sel[t, :, :, :150] = sel[t - 1, :, :, 150:]
+        for r in range(w.n_requests):
+            for l in range(w.n_layers):
+                keep = set(sel[t, r, l, :150].tolist())
+                fresh = [p for p in np.random.default_rng(t * 97 + r).permutation(w.n_positions)
+                         if p not in keep][:150]
+                sel[t, r, l, 150:] = fresh
+    orc = _oracles(w)
+    with hs.Pool.for_workload(w) as pool:
+        fill_selected(pool, w, sel)
+        out = torch.empty((w.n_requests, w.k), dtype=torch.int32, device="cuda")
+        for t in range(w.steps):
+            for l in range(w.n_layers):
+                pool.resolve(l, torch.from_numpy(np.ascontiguousarray(sel[t, :, l])).cuda(), out)
+                got = out.cpu().numpy()
+                for r in range(w.n_requests):
+                    rc, o, _ = orc[(r, l)].resolve(sel[t, r, l], out_base=r * w.slots)
+                    assert rc == OK and np.array_equal(got[r], o), (cluster, t, r, l)
+        for (r, l), p in orc.items():
+            check_metadata(pool, w, l, r, p, w.steps)
+            check_cache(pool, w, l, r, p.slot_pos)
+
+
 def test_largest_supported_slots_and_rejection():
     w = _small(n_requests=2, n_layers=1, k=2048, slots=14000, n_positions=60000,
                record_bytes=64, steps=6)

@@ -174,7 +174,9 @@ int hs_create_pool(const hs_pool_desc *desc, hs_pool **out) {
     p->dp.B = d.slots;
     p->dp.W = d.record_bytes;
     p->dp.L = d.n_positions;
-    if (!cuda_ok(hs::prepare_kernels(need))) { rc = HS_ERR_CUDA; goto fail; }
+    // the kernels' dynamic shared memory limit is a per-function setting
+    // shared by every pool: raise it to the device maximum, never lower it
+    if (!cuda_ok(hs::prepare_kernels((size_t)smem_optin))) { rc = HS_ERR_CUDA; goto fail; }
     rc = reset_state(p);
     if (rc != HS_OK) goto fail;
     *out = p;

@@ -300,6 +300,28 @@ def test_cuda_graph_replay_matches_oracle():
             check_cache(pool, w, l, r, p.slot_pos, sample=256)
 
 
+def test_pools_of_different_sizes_coexist():
+    """A small pool created after a large one must not shrink the large
+    pool's launch limits."""
+    big = _small(n_requests=2, n_layers=1, k=2048, slots=4096, n_positions=20000,
+                 record_bytes=64, steps=3)
+    small = _small(n_requests=2, n_layers=1, k=16, slots=32, n_positions=500, steps=3)
+    sel_b, sel_s = _random_trace(big, seed=1), _random_trace(small, seed=2)
+    with hs.Pool.for_workload(big) as pb, hs.Pool.for_workload(small) as ps:
+        fill_selected(pb, big, sel_b)
+        fill_selected(ps, small, sel_s)
+        ob = torch.empty((2, big.k), dtype=torch.int32, device="cuda")
+        os_ = torch.empty((2, small.k), dtype=torch.int32, device="cuda")
+        orc_b, orc_s = _oracles(big), _oracles(small)
+        for t in range(3):
+            pb.resolve(0, torch.from_numpy(np.ascontiguousarray(sel_b[t, :, 0])).cuda(), ob)
+            ps.resolve(0, torch.from_numpy(np.ascontiguousarray(sel_s[t, :, 0])).cuda(), os_)
+            gb, gs = ob.cpu().numpy(), os_.cpu().numpy()
+            for r in range(2):
+                assert np.array_equal(gb[r], orc_b[(r, 0)].resolve(sel_b[t, r, 0], out_base=r * big.slots)[1])
+                assert np.array_equal(gs[r], orc_s[(r, 0)].resolve(sel_s[t, r, 0], out_base=r * small.slots)[1])
+
+
 def test_link_probe_reports_bandwidth():
     h2d, gather = hs.hs_link_probe(256 << 20, reps=3, record_bytes=1152)
     assert h2d > 1.0 and gather > 1.0

@@ -19,7 +19,7 @@ CSRC = os.path.join(_PKG, "csrc")
 INCLUDE = os.path.join(_ROOT, "include")
 BUILD = os.path.join(_PKG, "_build")
 LIB = os.path.join(BUILD, "libhs.so")
-SOURCES = ("api.cu", "resolve.cu", "copy.cu")
+SOURCES = ("api.cu", "resolve.cu", "copy.cu", "noalloc.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 _lock = threading.Lock()
@@ -114,9 +114,19 @@ class Views(ctypes.Structure):
                 ("lru", ctypes.c_void_p), ("resolves", ctypes.c_void_p)]
 
 
+class LayerState(ctypes.Structure):
+    _fields_ = [("n_requests", ctypes.c_int32), ("n_positions", ctypes.c_int64),
+                ("record_bytes", ctypes.c_int32), ("slots", ctypes.c_int32),
+                ("host_records", ctypes.c_void_p), ("cache", ctypes.c_void_p),
+                ("page_table", ctypes.c_void_p), ("slot_pos", ctypes.c_void_p),
+                ("stamps", ctypes.c_void_p), ("lru", ctypes.c_void_p),
+                ("resolves", ctypes.c_void_p)]
+
+
 EXPORTS = ("hs_create_pool", "hs_destroy_pool", "hs_host_records", "hs_device_views",
            "hs_resolve", "hs_plan_bytes", "hs_prefetch_plan", "hs_prefetch_copy",
-           "hs_stats", "hs_reset", "hs_link_probe", "hs_kernels_per_call", "hs_strerror")
+           "hs_stats", "hs_reset", "hs_link_probe", "hs_kernels_per_call", "hs_strerror",
+           "hs_resolve_noalloc")
 
 
 def _declare(lib):
@@ -137,6 +147,8 @@ def _declare(lib):
                            ctypes.POINTER(ctypes.c_double)], ctypes.c_int),
         "hs_kernels_per_call": ([], i32),
         "hs_strerror": ([ctypes.c_int], ctypes.c_char_p),
+        "hs_resolve_noalloc": ([ctypes.POINTER(LayerState), i32, vp, vp, i32, vp, vp, vp],
+                               ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)

@@ -150,6 +150,25 @@ def hs_link_probe(nbytes: int, reps: int = 10, record_bytes: int = 1152):
     return a.value, b.value
 
 
+HS_NOALLOC_MAX_REQUESTS = 4096
+
+
+def hs_resolve_noalloc(state: dict, n_req, req_ids, sel, k, out, status=None, stream=None) -> None:
+    """Resolve one layer whose state the caller owns, allocating nothing.
+
+    ``state`` maps the hs_layer_state fields to values: sizes as ints,
+    arrays as torch tensors or device addresses.  See include/hs.h for the
+    scratch array it shares between calls."""
+    st = _native.LayerState(
+        state["n_requests"], state["n_positions"], state["record_bytes"], state["slots"],
+        _ptr(state["host_records"]), _ptr(state["cache"]), _ptr(state["page_table"]),
+        _ptr(state["slot_pos"]), _ptr(state["stamps"]), _ptr(state["lru"]),
+        _ptr(state["resolves"]))
+    _check(_lib().hs_resolve_noalloc(ctypes.byref(st), n_req, _ptr(req_ids), _ptr(sel), k,
+                                     _ptr(out), _ptr(status), _stream(stream)),
+           "hs_resolve_noalloc")
+
+
 class _CudaArray:
     def __init__(self, ptr, shape, typestr):
         self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr,

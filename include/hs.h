@@ -226,6 +226,65 @@ int32_t hs_kernels_per_call(void);
 /* Static description of an error code. */
 const char *hs_strerror(int code);
 
+/* ---- resolve without allocating --------------------------------------- */
+
+/* Largest request count hs_resolve_noalloc accepts. */
+#define HS_NOALLOC_MAX_REQUESTS 4096
+
+/* One layer's state, owned and allocated by the caller.  Initial (empty)
+ * state: every page_table and slot_pos entry -1, stamps 0, lru[r][b] = b,
+ * resolves 0 -- the state hs_create_pool gives its own arrays. */
+typedef struct {
+    int32_t n_requests;        /* R: request rows (1 .. HS_NOALLOC_MAX_REQUESTS) */
+    int64_t n_positions;       /* L_ctx (1 .. 2^31-1) */
+    int32_t record_bytes;      /* W: a multiple of 16 */
+    int32_t slots;             /* B (1 .. 32767) */
+    const void *host_records;  /* device-readable address of the records,
+                                  [R][L_ctx][W]: record (r, pos) at byte
+                                  (r * L_ctx + pos) * W, e.g. mapped pinned
+                                  host memory */
+    void *cache;               /* [R*B][W] slot contents */
+    int32_t *page_table;       /* [R][L_ctx] */
+    int32_t *slot_pos;         /* [R][B] */
+    uint32_t *stamps;          /* [R][B] */
+    uint16_t *lru;             /* [R][B] */
+    uint32_t *resolves;        /* [R] */
+} hs_layer_state;
+
+/*
+ * hs_resolve for one layer whose state the caller owns, without allocating
+ * anything.  The pages have no counterpart to this call; it exists for
+ * callers that cannot allocate device memory at the point where they
+ * resolve: serving engines that hand all free device memory to their own
+ * caching allocator at start-up (a cudaMalloc behind its back fails or
+ * fragments that reserve), and latency-critical loops where cudaMalloc and
+ * cudaFree would synchronise the device and stall every stream.
+ *
+ * Computation and output are those of hs_resolve (same kernel, same
+ * d_req_ids / d_sel / k / d_out conventions, no plan).  The per-request
+ * claim flags and counters that a pool keeps in its own device memory live
+ * here in one fixed scratch array compiled into the library: room for
+ * HS_NOALLOC_MAX_REQUESTS requests, held by every device that loads the
+ * library until the process exits.  The first call on a device looks up
+ * that array's device address (cudaGetSymbolAddress) and configures the
+ * kernel; make that first call before any stream capture on the device.
+ * Each call clears the part of the array it uses (an asynchronous memset on
+ * `stream`) before launching, and every call shares the array: calls that
+ * overlap on the GPU, on any streams, race.  Per-call counters are not
+ * reported.
+ *
+ * d_status: NULL, or a device u32 into which the kernel ORs HS_STATUS_* bits
+ *   for rejected requests (never cleared by the call).
+ * Errors: HS_ERR_INVALID_ARG (NULL state/arrays/d_sel/d_out, fields out of
+ * range, n_req > R, k outside [1, B]); HS_ERR_UNSUPPORTED (R above
+ * HS_NOALLOC_MAX_REQUESTS, or B and k needing more shared memory than a CTA
+ * has); HS_ERR_CUDA.  No cudaMalloc, cudaFree or allocating library routine
+ * is called.
+ */
+int hs_resolve_noalloc(const hs_layer_state *state, int32_t n_req, const int32_t *d_req_ids,
+                       const int32_t *d_sel, int32_t k, int32_t *d_out, uint32_t *d_status,
+                       void *stream);
+
 #ifdef __cplusplus
 }
 #endif

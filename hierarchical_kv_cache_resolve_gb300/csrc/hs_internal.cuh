@@ -66,48 +66,65 @@ __host__ __device__ inline size_t plan_bytes(int n_req, int k) {
     return 16 + (size_t)n_req * plan_entry_bytes(k);
 }
 
+// Hash table over the selected positions: 32-bit keys (position + 1, 0 =
+// empty) and 16-bit selection indices, at most a quarter full.
 __host__ __device__ inline int hash_capacity(int k) {
-    int h = 32;
-    while (h < 2 * k) h <<= 1;
+    int h = 64;
+    while (h < 4 * k) h <<= 1;
     return h;
+}
+
+// Membership bitmap over positions: one bit per position while L <= 2^17
+// (exact), otherwise 2^17 bits indexed by a hash of the position (a filter
+// in front of the hash table).
+constexpr int kMaxBitmapBits = 1 << 17;
+__host__ __device__ inline int bitmap_bits(int64_t L) {
+    int m = 1024;
+    while (m < kMaxBitmapBits && (int64_t)m < L) m <<= 1;
+    return m;
 }
 
 __host__ __device__ inline uint32_t align16(uint32_t x) { return (x + 15u) & ~15u; }
 
-// Shared-memory layout of the resolve / plan kernels for (B, k).
+// Shared-memory layout of the resolve / plan kernels for (B, k, L).
 struct SmemLayout {
     uint32_t hdr;      // header words + per-warp scan sums
-    uint32_t hash;     // u64[H]; after the probe it holds neworder u16[B]
+    uint32_t keys;     // u32[H]; after the probe it holds neworder u16[B]
+    uint32_t kidx;     // u16[H] selection index of each key
+    uint32_t bitmap;   // u32[M/32] membership bits
     uint32_t sel;      // i32[k]
     uint32_t hit;      // i32[k]: slot of a hit, -1 before ranking, -2-rank for misses
     uint32_t spos;     // i32[B]
     uint32_t order;    // u16[B]
     uint32_t flags;    // u8[B]: bit0 hit, bit1 victim
-    uint32_t vrank;    // u16[B]: rank of a victim slot among the victims
+    uint32_t vrank;    // u16[B]: rank of a victim slot (plan consumption only)
     uint32_t mpos;     // i32[k]: miss positions by rank
     uint32_t mslot;    // i32[k]: victims by rank
     uint32_t fpos;     // i32[2k]: fetch list when a plan is consumed
     uint32_t fslot;    // i32[2k]
     uint32_t total;
-    int H;
+    int H, M;
 };
 
-__host__ __device__ inline SmemLayout smem_layout(int B, int k, bool with_plan) {
+__host__ __device__ inline SmemLayout smem_layout(int B, int k, bool with_plan, int64_t L) {
     SmemLayout s;
     uint32_t o = 0;
     s.H = hash_capacity(k);
-    s.hdr = o;   o += 256;
-    s.hash = o;  { uint32_t a = 8u * s.H, b = 2u * B; o += align16(a > b ? a : b); }
-    s.sel = o;   o += align16(4u * k);
-    s.hit = o;   o += align16(4u * k);
-    s.spos = o;  o += align16(4u * B);
-    s.order = o; o += align16(2u * B);
-    s.flags = o; o += align16(1u * B);
-    s.vrank = o; o += align16(2u * B);
-    s.mpos = o;  o += align16(4u * k);
-    s.mslot = o; o += align16(4u * k);
-    s.fpos = o;  o += with_plan ? align16(8u * k) : 0;
-    s.fslot = o; o += with_plan ? align16(8u * k) : 0;
+    s.M = bitmap_bits(L);
+    s.hdr = o;    o += 256;
+    s.keys = o;   { uint32_t a = 4u * s.H, b = 2u * B; o += align16(a > b ? a : b); }
+    s.kidx = o;   o += align16(2u * s.H);
+    s.bitmap = o; o += align16((uint32_t)s.M / 8u);
+    s.sel = o;    o += align16(4u * k);
+    s.hit = o;    o += align16(4u * k);
+    s.spos = o;   o += align16(4u * B);
+    s.order = o;  o += align16(2u * B);
+    s.flags = o;  o += align16(1u * B);
+    s.vrank = o;  o += with_plan ? align16(2u * B) : 0;
+    s.mpos = o;   o += align16(4u * k);
+    s.mslot = o;  o += align16(4u * k);
+    s.fpos = o;   o += with_plan ? align16(8u * k) : 0;
+    s.fslot = o;  o += with_plan ? align16(8u * k) : 0;
     s.total = o;
     return s;
 }

@@ -129,8 +129,15 @@ __device__ __forceinline__ void copy_to_smem(void *dst, const void *src, int nby
         reinterpret_cast<uint16_t *>(d)[i] = reinterpret_cast<const uint16_t *>(s)[i];
 }
 
-__device__ __forceinline__ uint32_t hash_pos(int32_t pos, int H) {
-    return ((uint32_t)pos * 2654435761u) & (uint32_t)(H - 1);
+// Multiplicative (Fibonacci) hashing: the top bits of pos * 2^32/phi.
+__device__ __forceinline__ uint32_t hash_slot(int32_t pos, int shift) {
+    return ((uint32_t)pos * 2654435761u) >> shift;
+}
+
+// Bit of `pos` in the membership bitmap: the position itself when the
+// bitmap covers [0, L), otherwise a second multiplicative hash.
+__device__ __forceinline__ uint32_t member_bit(int32_t pos, bool exact, int mshift) {
+    return exact ? (uint32_t)pos : ((uint32_t)pos * 0x85EBCA77u) >> mshift;
 }
 
 // Copies F records: fetch-list entry j moves host_pair[fp[j]] to
@@ -198,11 +205,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const uint8_t *__restrict__ plan_in, uint8_t *__restrict__ plan_out) {
     extern __shared__ __align__(16) uint8_t smem[];
     const bool with_plan = !kPlanOnly && plan_in != nullptr;
-    const SmemLayout sl = smem_layout(p.B, k, with_plan);
+    const SmemLayout sl = smem_layout(p.B, k, with_plan, p.L);
     uint32_t *hdr = reinterpret_cast<uint32_t *>(smem + sl.hdr);
     uint32_t *sums = hdr + H_SUMS;
-    unsigned long long *tab = reinterpret_cast<unsigned long long *>(smem + sl.hash);
-    uint16_t *neworder = reinterpret_cast<uint16_t *>(smem + sl.hash);
+    uint32_t *keys = reinterpret_cast<uint32_t *>(smem + sl.keys);
+    uint16_t *kidx = reinterpret_cast<uint16_t *>(smem + sl.kidx);
+    uint32_t *bitmap = reinterpret_cast<uint32_t *>(smem + sl.bitmap);
+    uint16_t *neworder = reinterpret_cast<uint16_t *>(smem + sl.keys);
     int32_t *sel_s = reinterpret_cast<int32_t *>(smem + sl.sel);
     int32_t *hit_s = reinterpret_cast<int32_t *>(smem + sl.hit);
     int32_t *spos_s = reinterpret_cast<int32_t *>(smem + sl.spos);
@@ -219,6 +228,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t csize = kPlanOnly ? 1u : cluster_nctarank();
     const int ireq = (int)(blockIdx.x / csize);
     const int B = p.B, H = sl.H, W = p.W;
+    const int hshift = 33 - __ffs(H);          // 32 - log2(H)
+    const int mshift = 33 - __ffs(sl.M);       // 32 - log2(M)
+    const bool exact_bits = p.L <= (int64_t)sl.M;
     const int32_t *selr = sel_g + (int64_t)ireq * k;
 
     if (tid < H_SUMS) hdr[tid] = 0u;
@@ -241,7 +253,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             copy_to_smem(spos_s, p.slot_pos + pair * B, 4 * B);
             copy_to_smem(order_s, p.lru + pair * B, 2 * B);
         }
-        for (int h = tid; h < H; h += kThreads) tab[h] = 0ull;
+        {
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+            uint4 *kz = reinterpret_cast<uint4 *>(keys);
+            for (int i = tid; i < H / 4; i += kThreads) kz[i] = z;
+            uint4 *bz = reinterpret_cast<uint4 *>(bitmap);
+            for (int i = tid; i < sl.M / 128; i += kThreads) bz[i] = z;
+        }
         uint32_t a0 = 0, t0 = 0;
         if (tid == 0) {
             if (!r_ok) {
@@ -256,18 +274,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         cp_async_wait_all();
         __syncthreads();  // header zeroed, shared copies landed
+
+        // ---------------- P1: validate, hash build, membership bits ------
         {
             uint32_t bad = 0;
             if (tid == 0) {
                 bad = a0;
                 hdr[H_T] = t0;
             }
-            for (int i = tid; i < k; i += kThreads) {
-                const int32_t v = sel_s[i];
-                hit_s[i] = -1;
-                if (v < 0 || (int64_t)v >= p.L) bad |= HS_STATUS_POS_RANGE;
-            }
             if (r_ok) {
+                for (int i = tid; i < k; i += kThreads) {
+                    const int32_t v = sel_s[i];
+                    hit_s[i] = -1;
+                    if (v < 0 || (int64_t)v >= p.L) {
+                        bad |= HS_STATUS_POS_RANGE;
+                        continue;
+                    }
+                    const uint32_t mb = member_bit(v, exact_bits, mshift);
+                    atomicOr(&bitmap[mb >> 5], 1u << (mb & 31));
+                    uint32_t h = hash_slot(v, hshift);
+                    for (int probe = 0; probe < H; ++probe) {
+                        const uint32_t old = atomicCAS(&keys[h], 0u, (uint32_t)v + 1u);
+                        if (old == 0u) {
+                            kidx[h] = (uint16_t)i;
+                            break;
+                        }
+                        if (old == (uint32_t)v + 1u) {
+                            bad |= HS_STATUS_POS_DUP;
+                            break;
+                        }
+                        h = (h + 1) & (uint32_t)(H - 1);
+                    }
+                }
                 for (int b = tid; b < B; b += kThreads) {
                     const int32_t v = spos_s[b];
                     flags_s[b] = 0;
@@ -278,93 +316,134 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (bad) atomicOr(&hdr[H_ABORT], bad);
         }
         __syncthreads();
-
-        // ---------------- P1: hash build --------------------------------
-        if (hdr[H_ABORT] == 0u) {
-            for (int i = tid; i < k; i += kThreads) {
-                const int32_t key = sel_s[i];
-                const unsigned long long e =
-                    ((unsigned long long)(uint32_t)(key + 1) << 32) | (uint32_t)i;
-                uint32_t h = hash_pos(key, H);
-                for (int probe = 0; probe < H; ++probe) {
-                    const unsigned long long old = atomicCAS(&tab[h], 0ull, e);
-                    if (old == 0ull) break;
-                    if ((uint32_t)(old >> 32) == (uint32_t)(key + 1)) {
-                        atomicOr(&hdr[H_ABORT], HS_STATUS_POS_DUP);
-                        break;
-                    }
-                    h = (h + 1) & (uint32_t)(H - 1);
-                }
-            }
-        }
-        __syncthreads();
         const uint32_t abort_bits = hdr[H_ABORT];
 
         if (abort_bits == 0u) {
             // ------------- P2: probe the slots --------------------------
-            for (int b = tid; b < B; b += kThreads) {
-                const int32_t pos = spos_s[b];
-                if (pos < 0) continue;
-                uint32_t h = hash_pos(pos, H);
-                for (int probe = 0; probe < H; ++probe) {
-                    const unsigned long long e = tab[h];
-                    if (e == 0ull) break;
-                    if ((uint32_t)(e >> 32) == (uint32_t)(pos + 1)) {
-                        hit_s[(uint32_t)e] = b;
-                        flags_s[b] = 1;
-                        break;
+            // a slot whose position has no membership bit is not selected;
+            // the others look their position up in the hash table
+            for (int b0 = tid; b0 < B; b0 += kThreads * 4) {
+                int32_t pv[4];
+                uint32_t in[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int b = b0 + u * kThreads;
+                    pv[u] = b < B ? spos_s[b] : -1;
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    in[u] = 0u;
+                    if (pv[u] >= 0) {
+                        const uint32_t mb = member_bit(pv[u], exact_bits, mshift);
+                        in[u] = (bitmap[mb >> 5] >> (mb & 31)) & 1u;
                     }
-                    h = (h + 1) & (uint32_t)(H - 1);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    if (!in[u]) continue;
+                    const int32_t pos = pv[u];
+                    uint32_t h = hash_slot(pos, hshift);
+                    for (int probe = 0; probe < H; ++probe) {
+                        const uint32_t key = keys[h];
+                        if (key == 0u) break;
+                        if (key == (uint32_t)pos + 1u) {
+                            hit_s[kidx[h]] = b0 + u * kThreads;
+                            flags_s[b0 + u * kThreads] = 1;
+                            break;
+                        }
+                        h = (h + 1) & (uint32_t)(H - 1);
+                    }
                 }
             }
             __syncthreads();
 
             // ------------- P3: misses and victims (ballot scans) --------
+            // warp w owns a contiguous block of 32*seg elements of each
+            // array; element order = warp, then round, then lane.  Loads of
+            // up to 8 rounds are issued before their ballots.
             const int segK = (k + kThreads - 1) / kThreads;
             const int segB = (B + kThreads - 1) / kThreads;
             const int baseK = warp * 32 * segK, baseB = warp * 32 * segB;
             const uint32_t lt = lanemask_lt();
             uint32_t cm = 0, cn = 0;
-            for (int s = 0; s < segK; ++s) {
-                const int i = baseK + s * 32 + lane;
-                cm += __popc(__ballot_sync(0xFFFFFFFFu, i < k && hit_s[i] < 0));
+            for (int s0 = 0; s0 < segK; s0 += 8) {
+                bool pr[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int i = baseK + (s0 + u) * 32 + lane;
+                    pr[u] = s0 + u < segK && i < k && hit_s[i] < 0;
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (s0 + u < segK) cm += __popc(__ballot_sync(0xFFFFFFFFu, pr[u]));
             }
-            for (int s = 0; s < segB; ++s) {
-                const int q = baseB + s * 32 + lane;
-                cn += __popc(__ballot_sync(0xFFFFFFFFu, q < B && !(flags_s[order_s[q]] & 1)));
+            for (int s0 = 0; s0 < segB; s0 += 8) {
+                int ob[8];
+                bool pr[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int q = baseB + (s0 + u) * 32 + lane;
+                    ob[u] = (s0 + u < segB && q < B) ? (int)order_s[q] : -1;
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) pr[u] = ob[u] >= 0 && !(flags_s[ob[u]] & 1);
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (s0 + u < segB) cn += __popc(__ballot_sync(0xFFFFFFFFu, pr[u]));
             }
             uint32_t total;
             const uint32_t base = warp_counts_exscan(cm | (cn << 16), sums, &total);
             const int m = (int)(total & 0xFFFFu);
             const int nh = (int)(total >> 16);
             uint32_t mr = base & 0xFFFFu, nr = base >> 16;
-            for (int s = 0; s < segK; ++s) {
-                const int i = baseK + s * 32 + lane;
-                const bool pr = i < k && hit_s[i] < 0;
-                const uint32_t bal = __ballot_sync(0xFFFFFFFFu, pr);
-                if (pr) {
-                    const uint32_t rank = mr + __popc(bal & lt);
-                    mpos[rank] = sel_s[i];
-                    hit_s[i] = -2 - (int32_t)rank;
+            for (int s0 = 0; s0 < segK; s0 += 8) {
+                bool pr[8];
+                int32_t sv[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int i = baseK + (s0 + u) * 32 + lane;
+                    pr[u] = s0 + u < segK && i < k && hit_s[i] < 0;
+                    sv[u] = pr[u] ? sel_s[i] : 0;
                 }
-                mr += __popc(bal);
-            }
-            for (int s = 0; s < segB; ++s) {
-                const int q = baseB + s * 32 + lane;
-                const int b = q < B ? (int)order_s[q] : 0;
-                const bool pr = q < B && !(flags_s[b] & 1);
-                const uint32_t bal = __ballot_sync(0xFFFFFFFFu, pr);
-                if (pr) {
-                    const uint32_t rank = nr + __popc(bal & lt);
-                    if ((int)rank < m) {
-                        mslot[rank] = b;
-                        flags_s[b] |= 2;
-                        vrank_s[b] = (uint16_t)rank;
-                    } else {
-                        neworder[rank - m] = (uint16_t)b;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    if (s0 + u >= segK) break;
+                    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, pr[u]);
+                    if (pr[u]) {
+                        const uint32_t rank = mr + __popc(bal & lt);
+                        mpos[rank] = sv[u];
+                        hit_s[baseK + (s0 + u) * 32 + lane] = -2 - (int32_t)rank;
                     }
+                    mr += __popc(bal);
                 }
-                nr += __popc(bal);
+            }
+            for (int s0 = 0; s0 < segB; s0 += 8) {
+                int ob[8];
+                bool pr[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int q = baseB + (s0 + u) * 32 + lane;
+                    ob[u] = (s0 + u < segB && q < B) ? (int)order_s[q] : -1;
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) pr[u] = ob[u] >= 0 && !(flags_s[ob[u]] & 1);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    if (s0 + u >= segB) break;
+                    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, pr[u]);
+                    if (pr[u]) {
+                        const uint32_t rank = nr + __popc(bal & lt);
+                        const int b = ob[u];
+                        if ((int)rank < m) {
+                            mslot[rank] = b;
+                            flags_s[b] |= 2;
+                            if (with_plan) vrank_s[b] = (uint16_t)rank;
+                        } else {
+                            neworder[rank - m] = (uint16_t)b;
+                        }
+                    }
+                    nr += __popc(bal);
+                }
             }
             if (tid == 0) {
                 hdr[H_M] = (uint32_t)m;
@@ -643,7 +722,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int32_t *gs = mslot;           // victim slot of each predicted miss, -1 = drop
             uint8_t *gbit = flags_s;
             int32_t *xp = spos_s;          // leader misses that were not predicted
-            int32_t *xs = reinterpret_cast<int32_t *>(tab);
+            int32_t *xs = reinterpret_cast<int32_t *>(keys);
             if (!abort) {
                 for (int j = tid; j < g; j += kThreads) {
                     const int32_t hsl = lhit[gi[j]];
@@ -697,7 +776,7 @@ cudaError_t prepare_kernels(size_t max_smem) {
 cudaError_t launch_resolve(const DevPool &p, int layer, int n_req, const int32_t *req_ids,
                            const int32_t *sel, int k, int32_t *out, const void *plan,
                            int cluster, cudaStream_t st) {
-    const SmemLayout sl = smem_layout(p.B, k, plan != nullptr);
+    const SmemLayout sl = smem_layout(p.B, k, plan != nullptr, p.L);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(n_req * cluster), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -716,7 +795,7 @@ cudaError_t launch_resolve(const DevPool &p, int layer, int n_req, const int32_t
 
 cudaError_t launch_plan(const DevPool &p, int layer, int n_req, const int32_t *req_ids,
                         const int32_t *sel, int k, void *plan, cudaStream_t st) {
-    const SmemLayout sl = smem_layout(p.B, k, false);
+    const SmemLayout sl = smem_layout(p.B, k, false, p.L);
     resolve_kernel<true><<<n_req, kThreads, sl.total, st>>>(
         p, layer, n_req, req_ids, sel, k, nullptr, nullptr, static_cast<uint8_t *>(plan));
     return cudaGetLastError();

@@ -174,7 +174,7 @@ def test_every_cluster_size(cluster, monkeypatch):
 
 
 def test_largest_supported_slots_and_rejection():
-    w = _small(n_requests=2, n_layers=1, k=2048, slots=14000, n_positions=60000,
+    w = _small(n_requests=2, n_layers=1, k=2048, slots=11000, n_positions=60000,
                record_bytes=64, steps=6)
     sel = _random_trace(w, seed=8)
     orc = _oracles(w)

@@ -124,7 +124,7 @@ int hs_create_pool(const hs_pool_desc *desc, hs_pool **out) {
     if (!cuda_ok(cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) ||
         !cuda_ok(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)))
         return HS_ERR_CUDA;
-    const size_t need = hs::smem_layout(d.slots, d.max_k, true, d.n_positions).total;
+    const size_t need = hs::resolve_smem_bytes(d.slots, d.max_k, true, d.n_positions);
     if (need > (size_t)smem_optin) return HS_ERR_UNSUPPORTED;
 
     hs_pool *p = new (std::nothrow) hs_pool();

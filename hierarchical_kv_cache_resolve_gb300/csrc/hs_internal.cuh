@@ -129,6 +129,37 @@ __host__ __device__ inline SmemLayout smem_layout(int B, int k, bool with_plan, 
     return s;
 }
 
+// A follower CTA of a resolve cluster needs none of the leader's arrays.
+// After the 256-byte header it keeps: the share entries each warp staged
+// (kStageMax per warp), one staged-bit word per block of 32 share entries,
+// the list (positions, slots) of misses it did not stage, and then the
+// staging area for whole records, `cap` records per warp.
+constexpr int kStageMax = 32;
+struct FollowerLayout {
+    uint32_t stg, sbits, xp, xs, stage;
+    int cap;
+};
+
+__host__ __device__ inline FollowerLayout follower_lists(int k) {
+    FollowerLayout f;
+    uint32_t o = 256;
+    f.stg = o;   o += 4u * kWarps * kStageMax;
+    f.sbits = o; o += align16(4u * (uint32_t)((k + 31) / 32));
+    f.xp = o;    o += align16(4u * (uint32_t)k);
+    f.xs = o;    o += align16(4u * (uint32_t)k);
+    f.stage = (o + 127u) & ~127u;
+    f.cap = 0;
+    return f;
+}
+
+// Dynamic shared memory of a resolve launch: the leader's layout, and never
+// less than what a follower's lists need.
+__host__ __device__ inline uint32_t resolve_smem_bytes(int B, int k, bool with_plan, int64_t L) {
+    const uint32_t a = smem_layout(B, k, with_plan, L).total;
+    const uint32_t b = follower_lists(k).stage;
+    return a > b ? a : b;
+}
+
 // header word indices (u32 at smem + hdr)
 enum Hdr : int {
     H_ABORT = 0,     // HS_STATUS_* bits that abort this request

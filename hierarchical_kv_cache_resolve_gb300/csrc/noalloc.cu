@@ -65,7 +65,8 @@ extern "C" int hs_resolve_noalloc(const hs_layer_state *st, int32_t n_req, const
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
         return HS_ERR_CUDA;
-    if (hs::smem_layout(s.slots, k, false, s.n_positions).total > (uint32_t)smem_optin) return HS_ERR_UNSUPPORTED;
+    if (hs::resolve_smem_bytes(s.slots, k, false, s.n_positions) > (uint32_t)smem_optin)
+        return HS_ERR_UNSUPPORTED;
     if (n_req == 0) return HS_OK;
 
     unsigned char *scratch = nullptr;

@@ -129,6 +129,54 @@ __device__ __forceinline__ void copy_to_smem(void *dst, const void *src, int nby
         reinterpret_cast<uint16_t *>(d)[i] = reinterpret_cast<const uint16_t *>(s)[i];
 }
 
+// Orders this thread's generic-proxy writes to shared memory (cp.async
+// included) before later async-proxy (bulk copy) reads of it.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Bulk (TMA engine) copy of `bytes` (a multiple of 16, both ends 16-byte
+// aligned) from shared memory to global memory, tracked by bulk groups.
+__device__ __forceinline__ void bulk_store(void *gdst, const void *ssrc, int bytes) {
+    const uint32_t s = (uint32_t)__cvta_generic_to_shared(ssrc);
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(s),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Waits until the committed bulk copies have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Programmatic dependent launch: wait for the grids this one depends on to
+// complete (and their writes to be visible), then let the next grid in the
+// stream start launching.  Both are no-ops without the launch attribute.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void allow_dependent_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t dynamic_smem_bytes() {
+    uint32_t r;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(r));
+    return r;
+}
+
+// A follower CTA's shared memory after the header, staging records into
+// whatever the launch provides beyond its lists (see follower_lists_end).
+__device__ __forceinline__ FollowerLayout follower_layout(int k, int W) {
+    FollowerLayout f = follower_lists(k);
+    const uint32_t total = dynamic_smem_bytes();
+    const int cap = total > f.stage ? (int)((total - f.stage) / ((uint32_t)kWarps * (uint32_t)W)) : 0;
+    f.cap = cap < kStageMax ? cap : kStageMax;
+    return f;
+}
+
 // Multiplicative (Fibonacci) hashing: the top bits of pos * 2^32/phi.
 __device__ __forceinline__ uint32_t hash_slot(int32_t pos, int shift) {
     return ((uint32_t)pos * 2654435761u) >> shift;
@@ -234,6 +282,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t *selr = sel_g + (int64_t)ireq * k;
 
     if (tid < H_SUMS) hdr[tid] = 0u;
+    // everything above touched only registers and shared memory; global
+    // inputs may be written by the previous grid in the stream
+    grid_dependency_wait();
+    allow_dependent_launch();
     if (crank == 0) copy_to_smem(sel_s, selr, 4 * k);  // independent of the request id
 
     const int r = req_ids ? req_ids[ireq] : ireq;
@@ -242,9 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint8_t *host_pair = p.host + ((int64_t)(r_ok ? r : 0) * p.NL + layer) * p.L * W;
     uint8_t *cache_pair = p.cache + pair * B * (int64_t)W;
 
-    // follower state (registers): predicted misses and their preloaded chunks
-    uint4 pre[kUnroll];
-    int npre = 0;
+    // follower state: records this warp staged (warp-uniform)
+    int staged_n = 0;
 
     if (crank == 0) {
         // ---------------- P0: load -------------------------------------
@@ -537,67 +588,54 @@ __global__ void __launch_bounds__(kThreads, 1)
             return;
         }
     } else if (!with_plan) {
-        // ---------------- follower F0-F2: predict misses, start the loads --
+        // ---------------- follower F0: predict misses, stage their records --
+        // Warp w takes blocks of 32 consecutive share entries (w, w + 16,
+        // ...).  A lane reads its selection and the page-table entry of the
+        // position; -1 predicts a miss.  For every predicted miss the warp
+        // issues cp.async copies of the record from the mapped host pool
+        // into its own staging area of shared memory, up to `cap` records;
+        // sbits[block] remembers which entries were staged.
+        const FollowerLayout fl = follower_layout(k, W);
+        int32_t *stg = reinterpret_cast<int32_t *>(smem + fl.stg) + warp * kStageMax;
+        uint32_t *sbits = reinterpret_cast<uint32_t *>(smem + fl.sbits);
+        uint8_t *stage = smem + fl.stage + (size_t)warp * fl.cap * W;
         const int nf = csize > 1 ? (int)csize - 1 : 1, f = (int)crank - 1;
         const int i0 = (int)((int64_t)f * k / nf), i1 = (int)((int64_t)(f + 1) * k / nf);
         const int ns = i1 - i0;
-        int32_t *gi = hit_s;     // predicted misses: selection index
-        int32_t *gp = mpos;      //                   position
-        uint8_t *gbit = flags_s; // prediction per share entry
-        copy_to_smem(sel_s, selr + i0, 4 * ns);
-        cp_async_wait_all();
-        __syncthreads();
+        const int nblk = (ns + 31) >> 5;
         const int32_t *pt = p.pt + pair * p.L;
-        const int seg = (ns + kThreads - 1) / kThreads;
-        const int base_e = warp * 32 * seg;
-        uint32_t cnt = 0;
-        for (int s0 = 0; s0 < seg; s0 += 8) {
-            int32_t ptv[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int e = base_e + (s0 + u) * 32 + lane;
-                ptv[u] = 0;
-                if (s0 + u < seg && e < ns && r_ok) {
-                    const int32_t pos = sel_s[e];
-                    if (pos >= 0 && (int64_t)pos < p.L) ptv[u] = pt[pos];
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                if (s0 + u >= seg) break;
-                const int e = base_e + (s0 + u) * 32 + lane;
-                const bool g = e < ns && ptv[u] == -1;
-                if (e < ns) gbit[e] = g ? 1 : 0;
-                cnt += __popc(__ballot_sync(0xFFFFFFFFu, g));
-            }
-        }
-        uint32_t total;
-        uint32_t rank = warp_counts_exscan(cnt, sums, &total);
-        const uint32_t lt = lanemask_lt();
-        for (int s = 0; s < seg; ++s) {
-            const int e = base_e + s * 32 + lane;
-            const bool g = e < ns && gbit[e];
-            const uint32_t bal = __ballot_sync(0xFFFFFFFFu, g);
-            if (g) {
-                const uint32_t j = rank + __popc(bal & lt);
-                gi[j] = i0 + e;
-                gp[j] = sel_s[e];
-            }
-            rank += __popc(bal);
-        }
-        if (tid == 0) hdr[H_G] = total;
-        __syncthreads();
         const int CW = W >> 4;
-        const int Q = (int)total * CW;
+        for (int blk0 = warp; blk0 < nblk; blk0 += kWarps * 4) {
+            int32_t pos[4], ptv[4];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int q = tid + u * kThreads;
-            if (q < Q) {
-                const int j = q / CW;
-                pre[u] = ld_nc_v4(host_pair + (int64_t)gp[j] * W + (q - j * CW) * 16);
-                npre = u + 1;
+            for (int u = 0; u < 4; ++u) {
+                const int e = (blk0 + u * kWarps) * 32 + lane;
+                pos[u] = (blk0 + u * kWarps < nblk && e < ns) ? selr[i0 + e] : -1;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                ptv[u] = (r_ok && pos[u] >= 0 && (int64_t)pos[u] < p.L) ? pt[pos[u]] : 0;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int blk = blk0 + u * kWarps;
+                if (blk >= nblk) break;
+                uint32_t mask = __ballot_sync(0xFFFFFFFFu, ptv[u] == -1);
+                uint32_t staged = 0;
+                while (mask && staged_n < fl.cap) {
+                    const int src = __ffs(mask) - 1;
+                    mask &= mask - 1;
+                    const int32_t q = __shfl_sync(0xFFFFFFFFu, pos[u], src);
+                    uint8_t *dst = stage + (size_t)staged_n * W;
+                    const uint8_t *from = host_pair + (int64_t)q * W;
+                    for (int c = lane; c < CW; c += 32) cp_async16(dst + 16 * c, from + 16 * c);
+                    if (lane == 0) stg[staged_n] = blk * 32 + src;
+                    staged |= 1u << src;
+                    ++staged_n;
+                }
+                if (lane == 0) sbits[blk] = staged;
             }
         }
+        __syncthreads();
     }
 
     if constexpr (!kPlanOnly) {
@@ -707,56 +745,59 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fetch_records(host_pair, cache_pair, dp, ds, F, W, (int)(crank - 1) * kThreads + tid,
                               (int)(csize - 1) * kThreads);
         } else {
-            // ------------- follower F3-F6: apply the leader's verdict ----------
+            // ------------- follower F1-F3: apply the leader's verdict ----------
             cg::cluster_group cl = cg::this_cluster();
             const uint32_t *lh = cl.map_shared_rank(hdr, 0);
             const int32_t *lhit = cl.map_shared_rank(hit_s, 0);
             const int32_t *lmslot = cl.map_shared_rank(mslot, 0);
             const bool abort = lh[H_ABORT] != 0u;
+            const FollowerLayout fl = follower_layout(k, W);
+            const int32_t *stg = reinterpret_cast<const int32_t *>(smem + fl.stg) + warp * kStageMax;
+            const uint32_t *sbits = reinterpret_cast<const uint32_t *>(smem + fl.sbits);
+            const uint8_t *stage = smem + fl.stage + (size_t)warp * fl.cap * W;
+            int32_t *xp = reinterpret_cast<int32_t *>(smem + fl.xp);  // misses not staged
+            int32_t *xs = reinterpret_cast<int32_t *>(smem + fl.xs);
             const int nf = csize > 1 ? (int)csize - 1 : 1, f = (int)crank - 1;
             const int i0 = (int)((int64_t)f * k / nf), i1 = (int)((int64_t)(f + 1) * k / nf);
             const int ns = i1 - i0;
-            const int g = (int)hdr[H_G];
-            int32_t *gi = hit_s;
-            int32_t *gp = mpos;
-            int32_t *gs = mslot;           // victim slot of each predicted miss, -1 = drop
-            uint8_t *gbit = flags_s;
-            int32_t *xp = spos_s;          // leader misses that were not predicted
-            int32_t *xs = reinterpret_cast<int32_t *>(keys);
+            const int nblk = (ns + 31) >> 5;
+            // F1: the victim slot of each staged record (-1: the leader found
+            // a hit), and the leader's misses of this warp's blocks that were
+            // not staged
+            int32_t my_slot = -1;
+            if (!abort && lane < staged_n) {
+                const int32_t hsl = lhit[i0 + stg[lane]];
+                my_slot = hsl <= -2 ? lmslot[-2 - hsl] : -1;
+            }
             if (!abort) {
-                for (int j = tid; j < g; j += kThreads) {
-                    const int32_t hsl = lhit[gi[j]];
-                    gs[j] = hsl <= -2 ? lmslot[-2 - hsl] : -1;
-                }
-                for (int e = tid; e < ns; e += kThreads) {
-                    const int32_t hsl = lhit[i0 + e];
-                    if (hsl <= -2 && !gbit[e]) {
+                for (int blk = warp; blk < nblk; blk += kWarps) {
+                    const int e = blk * 32 + lane;
+                    const int32_t hsl = e < ns ? lhit[i0 + e] : -1;
+                    if (hsl <= -2 && !((sbits[blk] >> lane) & 1u)) {
                         const uint32_t x = atomicAdd(&hdr[H_NX], 1u);
-                        xp[x] = sel_s[e];
+                        xp[x] = selr[i0 + e];
                         xs[x] = lmslot[-2 - hsl];
                     }
                 }
             }
             __syncthreads();
             cluster_arrive_relaxed();  // phase B: done reading the leader
+            cp_async_wait_all();       // no copy into shared memory outlives the CTA
             if (!abort) {
-                const int CW = W >> 4;
-                const int Q = g * CW;
-#pragma unroll
-                for (int u = 0; u < kUnroll; ++u) {
-                    const int q = tid + u * kThreads;
-                    if (u < npre && q < Q) {
-                        const int j = q / CW;
-                        const int32_t slot = gs[j];
-                        if (slot >= 0)
-                            *reinterpret_cast<uint4 *>(cache_pair + (int64_t)slot * W +
-                                                       (q - j * CW) * 16) = pre[u];
-                    }
+                // F2: staged records have landed; one bulk copy per record
+                // from shared memory to its victim slot
+                fence_proxy_async_shared();
+                __syncwarp();
+                for (int s = 0; s < staged_n; ++s) {
+                    const int32_t slot = __shfl_sync(0xFFFFFFFFu, my_slot, s);
+                    if (lane == 0 && slot >= 0)
+                        bulk_store(cache_pair + (int64_t)slot * W, stage + (size_t)s * W, W);
                 }
-                fetch_records(host_pair, cache_pair, gp, gs, g, W, tid, kThreads,
-                              kUnroll * kThreads);
+                if (lane == 0) bulk_commit();
+                // F3: misses that were not staged
                 const int nx = (int)hdr[H_NX];
                 if (nx > 0) fetch_records(host_pair, cache_pair, xp, xs, nx, W, tid, kThreads);
+                if (lane == 0) bulk_wait_read();  // shared memory is read before the CTA ends
             }
         }
         cluster_wait();  // phase B: no CTA leaves while the leader is being read
@@ -776,19 +817,22 @@ cudaError_t prepare_kernels(size_t max_smem) {
 cudaError_t launch_resolve(const DevPool &p, int layer, int n_req, const int32_t *req_ids,
                            const int32_t *sel, int k, int32_t *out, const void *plan,
                            int cluster, cudaStream_t st) {
-    const SmemLayout sl = smem_layout(p.B, k, plan != nullptr, p.L);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(n_req * cluster), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = sl.total;
+    cfg.dynamicSmemBytes = resolve_smem_bytes(p.B, k, plan != nullptr, p.L);
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)cluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // the launch may overlap the tail of the previous grid in the stream;
+    // the kernel waits for that grid before touching global memory
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, resolve_kernel<false>, p, layer, n_req, req_ids, sel, k, out,
                               static_cast<const uint8_t *>(plan), static_cast<uint8_t *>(nullptr));
 }

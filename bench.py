@@ -44,6 +44,23 @@ METRIC = ("resolves/sec and miss-fetch GB/s (fraction of measured pinned H2D BW)
           "at 1 GB300")
 L2_FLUSH_BYTES = 256 << 20
 
+# Counters of one steady-state resolve launch from an ncu capture (summary in
+# profiles/resolve_kernel_dsa_mla_full.md), valid only for the kernel sources
+# they were taken on: reported as null once those sources change.
+PROFILED_SOURCES = {"resolve.cu": "6193d879b3c6135c", "hs_internal.cuh": "505751c1885465e7"}
+PROFILED_LAUNCH = {"dram_bytes": 874_496, "link_bytes": 2_073_600,
+                   "algorithmic_link_bytes": 2_073_600}
+
+
+def profiled_counters():
+    import hashlib
+    csrc = os.path.join(ROOT, "hierarchical_kv_cache_resolve_gb300", "csrc")
+    for name, digest in PROFILED_SOURCES.items():
+        with open(os.path.join(csrc, name), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest()[:16] != digest:
+                return None
+    return PROFILED_LAUNCH
+
 
 # ---------------------------------------------------------------- helpers ---
 
@@ -340,6 +357,7 @@ def run_gpu(args, w, rank, world, dist_on):
     pool.close()
 
     peaks = load_peaks()
+    prof = profiled_counters()
     hbm_peak = peaks.get("hbm_gbs") if peaks else None
     miss_gbs = total_fetched / dev_s_max / 1e9
     link_achieved = link_bytes_per_launch / avg_launch_s / 1e9
@@ -386,7 +404,12 @@ def run_gpu(args, w, rank, world, dist_on):
             "peak": h2d_gbs,
             "unit": "GB/s",
             "frac": link_achieved / h2d_gbs,
-            "traffic": None,
+            # ncu counters of one captured launch: DRAM read+write bytes (the
+            # spec's traffic) and the host-link (sysmem) read bytes, beside
+            # that launch's own algorithmic link bytes
+            "traffic": prof["dram_bytes"] if prof else None,
+            "link_traffic": prof["link_bytes"] if prof else None,
+            "traffic_launch_algorithmic_link_bytes": prof["algorithmic_link_bytes"] if prof else None,
             "peak_source": "pinned cudaMemcpyAsync H2D, 1 GiB, best of 10, this run",
             "algorithmic_bytes_per_launch": link_bytes_per_launch,
             "avg_launch_us": avg_launch_s * 1e6,
@@ -398,7 +421,7 @@ def run_gpu(args, w, rank, world, dist_on):
             "peak": hbm_peak,
             "unit": "GB/s",
             "frac": (hbm_achieved / hbm_peak) if hbm_peak else None,
-            "traffic": None,
+            "traffic": prof["dram_bytes"] if prof else None,
             "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if hbm_peak else None,
             "algorithmic_bytes_per_launch": hbm_per_launch,
         },
@@ -428,12 +451,18 @@ def main(argv=None):
     ap.add_argument("--workload", default="dsa_mla")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-threads", type=int, default=0)
+    ap.add_argument("--l-ctx", type=int, default=0,
+                    help="profiling captures only: shrink L_ctx (same k, B, W, batch), so "
+                         "that the pinned pool and page tables stay small")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
 
     from workloads import configs
     base = configs.BY_NAME[args.workload]
+    if args.l_ctx:
+        base = base.with_(n_positions=args.l_ctx,
+                          local_window=min(base.local_window, args.l_ctx // 8))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))

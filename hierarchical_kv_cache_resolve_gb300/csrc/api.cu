@@ -58,11 +58,11 @@ int reset_state(hs_pool *p) {
 }
 
 // Cluster size for a resolve over n_req requests: the largest power of two
-// up to 8 that keeps the grid within about two CTAs per SM.
+// up to 8 that keeps the grid in one wave (a resolve CTA occupies an SM).
 int pick_cluster(const hs_pool *p, int n_req) {
     if (p->cluster_override > 0) return p->cluster_override;
     int c = hs::kMaxCluster;
-    while (c > 1 && (int64_t)n_req * c > 2 * (int64_t)p->sm_count) c >>= 1;
+    while (c > 1 && (int64_t)n_req * c > (int64_t)p->sm_count) c >>= 1;
     return c;
 }
 

@@ -95,7 +95,7 @@ extern "C" int hs_resolve_noalloc(const hs_layer_state *st, int32_t n_req, const
     p.W = s.record_bytes;
     p.L = s.n_positions;
     int cluster = hs::kMaxCluster;
-    while (cluster > 1 && (int64_t)n_req * cluster > 2 * (int64_t)sms) cluster >>= 1;
+    while (cluster > 1 && (int64_t)n_req * cluster > (int64_t)sms) cluster >>= 1;
     const cudaError_t e = hs::launch_resolve(p, 0, n_req, d_req_ids, d_sel, k, d_out, nullptr,
                                              cluster, cs);
     return e == cudaSuccess ? HS_OK : HS_ERR_CUDA;

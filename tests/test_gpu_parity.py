@@ -126,6 +126,12 @@ def test_quest_pages_full():
 
 
 @pytest.mark.slow
+def test_quest_page_records_full():
+    """Page-granular records (64 KiB per record, k = 128 pages, B = 256)."""
+    run_and_compare(configs.QUEST_PAGE_RECORDS, meta_every=32, cache_sample=64)
+
+
+@pytest.mark.slow
 def test_tight_prefetch_full_with_prefetch():
     run_and_compare(configs.TIGHT_PREFETCH, meta_every=32, cache_sample=256, prefetch=True)
 

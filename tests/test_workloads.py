@@ -63,7 +63,8 @@ def test_fill_matches_gen_and_streams_differ():
 @pytest.mark.parametrize("w", [configs.TINY, configs.DSA_MLA.with_(steps=40),
                                configs.TIGHT_PREFETCH.with_(n_requests=2, steps=20),
                                configs.NO_LOCALITY.with_(steps=8),
-                               configs.QUEST_PAGES.with_(n_requests=2, steps=20)])
+                               configs.QUEST_PAGES.with_(n_requests=2, steps=20),
+                               configs.QUEST_PAGE_RECORDS.with_(n_requests=2, steps=20)])
 def test_trace_shape_range_distinct(w):
     s = traces.generate(w)
     assert s.shape == (w.steps, w.n_requests, w.n_layers, w.k) and s.dtype == np.int32

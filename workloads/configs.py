@@ -112,4 +112,11 @@ QUEST_PAGES = Workload(
     always_last_pages=4, zipf_s=1.1, score_drift=0.05)
 
 ALL = (TINY, DSA_MLA, TIGHT_PREFETCH, NO_LOCALITY, QUEST_PAGES)
-BY_NAME = {w.name: w for w in ALL}
+
+# Page-granular records: the Quest selection process over whole pages, each
+# page one 64 KiB record (16 tokens x 4096 B), k = 128 pages, B = 256 pages.
+QUEST_PAGE_RECORDS = QUEST_PAGES.with_(
+    name="quest_page_records", n_positions=2048, k=128, slots=256,
+    record_bytes=16 * 4096, page_tokens=1)
+
+BY_NAME = {w.name: w for w in ALL + (QUEST_PAGE_RECORDS,)}

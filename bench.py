@@ -44,9 +44,9 @@ METRIC = ("resolves/sec and miss-fetch GB/s (fraction of measured pinned H2D BW)
           "at 1 GB300")
 L2_FLUSH_BYTES = 256 << 20
 
-# Counters of one steady-state resolve launch from an ncu capture (summary in
-# profiles/resolve_kernel_dsa_mla_full.md), valid only for the kernel sources
-# they were taken on: reported as null once those sources change.
+# Counters of one steady-state resolve launch from an ncu capture (dsa_mla
+# shape, L_ctx cut to 16384: same batch, k, B, W), valid only for the kernel
+# sources they were taken on: reported as null once those sources change.
 PROFILED_SOURCES = {"resolve.cu": "6193d879b3c6135c", "hs_internal.cuh": "505751c1885465e7"}
 PROFILED_LAUNCH = {"dram_bytes": 874_496, "link_bytes": 2_073_600,
                    "algorithmic_link_bytes": 2_073_600}
@@ -440,6 +440,121 @@ def run_gpu(args, w, rank, world, dist_on):
     return res
 
 
+# ------------------------------------------------ exact prefetch overlap ----
+
+def run_prefetch_overlap(args, w):
+    """Exact layer-wise prefetch against stand-in compute.
+
+    Each layer of a decode step is its resolve followed by a bf16 GEMM that
+    stands in for the layer's attention and MLP (`--compute-us` long).  For
+    a layer that shares its anchor's selection, prefetch ON plans its misses
+    right after the anchor's resolve and copies them on a side stream, so the
+    copy overlaps the compute of the layers in between; its own resolve then
+    consumes the plan.  Three timings of the same steps (CUDA events, L2
+    flushed before each step): compute only, resolves without prefetch,
+    resolves with prefetch.  The share of the resolve time hidden is
+    1 - (on - compute) / (off - compute).
+    """
+    import torch
+
+    from hierarchical_kv_cache_resolve_gb300 import hs
+    from workloads import records, traces
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    R, NL, k, T = w.n_requests, w.n_layers, w.k, w.steps
+    sel = traces.generate(w)
+    dsel = torch.from_numpy(np.ascontiguousarray(sel.transpose(0, 2, 1, 3))).to(dev)
+    pool = hs.Pool.for_workload(w)
+    for r in range(R):
+        for l in range(NL):
+            records.fill(pool.host_records(r, l).ctypes.data, w, r, l)
+    out = torch.empty((NL, R, k), dtype=torch.int32, device=dev)
+    plans = {l: torch.empty(hs.hs_plan_bytes(R, k), dtype=torch.uint8, device=dev)
+             for l in range(NL) if w.anchors[l] != l}
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    main, side = torch.cuda.current_stream(), torch.cuda.Stream()
+
+    # stand-in compute: [4096 x 4096] x [4096 x n] bf16, n chosen for the target time
+    a = torch.randn(4096, 4096, device=dev, dtype=torch.bfloat16)
+    b = torch.randn(4096, 4096, device=dev, dtype=torch.bfloat16)
+    for _ in range(3):
+        a @ b
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(10):
+        a @ b
+    e1.record()
+    torch.cuda.synchronize()
+    us_full = e0.elapsed_time(e1) * 100.0
+    n = max(64, min(4096, int(4096 * args.compute_us / us_full) // 64 * 64))
+    bb = b[:, :n].contiguous()
+
+    def compute():
+        return a @ bb
+
+    def step(t, mode):
+        evs = {}
+        for l in range(NL):
+            anc = w.anchors[l]
+            if mode != "compute":
+                if l == anc:
+                    pool.resolve(l, dsel[t, l], out[l], stream=main)
+                    if mode == "on":
+                        for l2 in plans:
+                            if w.anchors[l2] != l:
+                                continue
+                            pool.prefetch_plan(l, l2, dsel[t, l2], plans[l2], stream=main)
+                            ev = torch.cuda.Event()
+                            ev.record(main)
+                            side.wait_event(ev)
+                            pool.prefetch_copy(l2, R, k, plans[l2], stream=side)
+                            evs[l2] = torch.cuda.Event()
+                            evs[l2].record(side)
+                elif mode == "on":
+                    main.wait_event(evs[l])
+                    pool.resolve(l, dsel[t, l], out[l], plan=plans[l], stream=main)
+                else:
+                    pool.resolve(l, dsel[t, l], out[l], stream=main)
+            compute()
+
+    results = {}
+    for mode in ("compute", "off", "on"):
+        pool.reset()
+        for s in range(args.warmup):
+            step(s % T, mode)
+        torch.cuda.synchronize()
+        total = 0.0
+        for i in range(args.steps):
+            flush.fill_(i)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(main)
+            step((args.warmup + i) % T, mode)
+            e1.record(main)
+            torch.cuda.synchronize()
+            total += e0.elapsed_time(e1)
+        results[mode] = total / args.steps
+        if mode != "compute":
+            st = pool.stats(check=False)
+            results[mode + "_stats"] = {x: st[x] for x in ("misses", "fetched_bytes",
+                                                          "prefetched_bytes", "plan_hits",
+                                                          "plan_mismatches", "status")}
+    pool.close()
+    hidden = 1.0 - (results["on"] - results["compute"]) / (results["off"] - results["compute"])
+    shared = sum(1 for l in range(NL) if w.anchors[l] != l)
+    return {
+        "metric": "exact-prefetch overlap: step time with resolves, without and with prefetch",
+        "value": hidden, "unit": "fraction of resolve time hidden",
+        "higher_is_better": True,
+        "config": {"workload": workload_name(w), "shared_layers_per_step": shared,
+                   "compute_stand_in": f"bf16 GEMM 4096x4096x{n} after every layer",
+                   "l2": "flushed before every timed step"},
+        "ms_per_step": {"compute_only": results["compute"], "prefetch_off": results["off"],
+                        "prefetch_on": results["on"]},
+        "counters": {"off": results["off_stats"], "on": results["on_stats"]},
+        "steps": args.steps, "warmup": args.warmup,
+    }
+
+
 # ------------------------------------------------------------------ main ----
 
 def main(argv=None):
@@ -454,6 +569,13 @@ def main(argv=None):
     ap.add_argument("--l-ctx", type=int, default=0,
                     help="profiling captures only: shrink L_ctx (same k, B, W, batch), so "
                          "that the pinned pool and page tables stay small")
+    ap.add_argument("--requests", type=int, default=0,
+                    help="override the workload's batch (requests per launch)")
+    ap.add_argument("--prefetch-overlap", action="store_true",
+                    help="measure exact layer-wise prefetch against stand-in compute "
+                         "(a workload with shared layers, e.g. tight_prefetch)")
+    ap.add_argument("--compute-us", type=float, default=60.0,
+                    help="stand-in compute per layer for --prefetch-overlap")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -463,6 +585,8 @@ def main(argv=None):
     if args.l_ctx:
         base = base.with_(n_positions=args.l_ctx,
                           local_window=min(base.local_window, args.l_ctx // 8))
+    if args.requests:
+        base = base.with_(n_requests=args.requests)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -501,6 +625,10 @@ def main(argv=None):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     w = rank_workload(base, rank)
+    if args.prefetch_overlap:
+        if rank == 0:
+            print(json.dumps(run_prefetch_overlap(args, w)))
+        return 0
     res = run_gpu(args, w, rank, world, dist_on)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:

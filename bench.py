@@ -47,7 +47,7 @@ L2_FLUSH_BYTES = 256 << 20
 # Counters of one steady-state resolve launch from an ncu capture (dsa_mla
 # shape, L_ctx cut to 16384: same batch, k, B, W), valid only for the kernel
 # sources they were taken on: reported as null once those sources change.
-PROFILED_SOURCES = {"resolve.cu": "6193d879b3c6135c", "hs_internal.cuh": "505751c1885465e7"}
+PROFILED_SOURCES = {"resolve.cu": "56b273a99f480fdf", "hs_internal.cuh": "505751c1885465e7"}
 PROFILED_LAUNCH = {"dram_bytes": 874_496, "link_bytes": 2_073_600,
                    "algorithmic_link_bytes": 2_073_600}
 

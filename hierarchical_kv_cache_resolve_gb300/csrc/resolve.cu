@@ -6,31 +6,33 @@
 //
 // CTA 0 of a cluster (the leader) owns the request's metadata:
 //   P0  cp.async the k selections, the slot map and the LRU order into shared
-//       memory; reject positions outside [0, L) and corrupt metadata;
-//   P1  insert the selections into a shared-memory open-addressing hash
-//       table (key = position, value = selection index); a repeated key is
-//       a duplicate selection;
-//   P2  probe every slot's position against the table: a found slot is a
-//       hit for that selection index;
+//       memory, zero the hash table and the position bitmap;
+//   P1  reject positions outside [0, L), repeated positions and corrupt
+//       metadata; insert every selection into a shared-memory open-addressing
+//       table (32-bit key = position + 1, 16-bit selection index beside it,
+//       at most a quarter full) and set its bit in the position bitmap;
+//   P2  probe every slot's position: no bit means not selected, otherwise
+//       the table gives the selection index the slot is a hit for;
 //   P3  one warp-ballot scan over the selections (misses in selection order)
-//       fused with one over the LRU order (non-hit slots in (stamp, slot)
-//       order): the j-th miss gets the j-th non-hit slot as its victim;
+//       and one over the LRU order (non-hit slots in (stamp, slot) order):
+//       the j-th miss gets the j-th non-hit slot as its victim;
 //   P4  publish slots, update page table / slot map / stamps, and rebuild
-//       the LRU order with a second ballot scan over the slots.
+//       the LRU order with a third ballot scan over the slots.
 //
 // CTAs 1..C-1 (the followers) move the data.  Follower f owns a contiguous
-// share of the selection indices.  Before the leader has decided anything it
-// predicts which of its selections miss from the page table (a position
-// with no slot is a miss), compacts them and issues the 16-byte
-// non-coherent loads of those host records into registers, so that the
-// host-link transfer overlaps the leader's P0-P3.  After the cluster barrier
-// it reads the leader's verdict through distributed shared memory: every
-// predicted miss gets its victim slot (or is dropped if the leader found a
-// hit), and any miss of its share it did not predict is fetched as well, so
-// the leader's decision is always the one applied.  The leader commits the
-// metadata (P4) while the followers store.  A cluster of one CTA does all
-// of it in the leader, fetch after P3.  A resolve that consumes a prefetch
-// plan uses the leader's fetch list instead of the prediction.
+// share of the selection indices.  Before the leader has decided anything
+// each warp predicts which of its selections miss from the page table (a
+// position with no slot will miss) and stages those records from the mapped
+// host pool into its shared memory with cp.async, so that the host-link
+// transfer overlaps the leader's P0-P3.  After the cluster barrier it reads
+// the leader's verdict through distributed shared memory: each staged record
+// goes to its victim slot with one bulk (TMA) copy, or is dropped if the
+// leader found a hit, and any miss of its share that was not staged is
+// fetched with 16-byte non-coherent loads, so the leader's decision is
+// always the one applied.  The leader commits the metadata (P4) while the
+// followers store.  A cluster of one CTA does all of it in the leader, fetch
+// after P3.  A resolve that consumes a prefetch plan uses the leader's fetch
+// list instead of the prediction.
 //
 // Victim selection without sorting: the LRU order array is kept sorted by
 // (stamp, slot).  A resolve at step t keeps the untouched slots in their old

@@ -92,6 +92,36 @@ def test_bad_request_ids_and_empty_call():
         assert pool.stats(1)["resolves"] == 1
 
 
+def test_request_resolved_twice_in_one_launch_is_detected():
+    """Two rows naming the same request race for it: one claims the pair and
+    resolves it, the other is refused (-1, HS_STATUS_REQ_BUSY) and changes
+    nothing."""
+    w = _small(n_requests=2, n_layers=1, k=200, slots=400, n_positions=20000, steps=1)
+    sel = _random_trace(w, seed=9)
+    with hs.Pool.for_workload(w) as pool:
+        fill_selected(pool, w, sel)
+        one = np.ascontiguousarray(sel[0, 1, 0])
+        s = torch.from_numpy(np.stack([one, one])).cuda()
+        ids = torch.tensor([1, 1], dtype=torch.int32, device="cuda")
+        out = torch.empty((2, w.k), dtype=torch.int32, device="cuda")
+        pool.resolve(0, s, out, req_ids=ids)
+        st = pool.stats(0, check=False)
+        got = out.cpu().numpy()
+        refused = [i for i in range(2) if (got[i] == -1).all()]
+        p = Pair(w.slots, w.n_positions, w.record_bytes)
+        _, want, _ = p.resolve(one, out_base=1 * w.slots)
+        if st["status"] & hs.HS_STATUS_REQ_BUSY:
+            assert len(refused) == 1
+            assert np.array_equal(got[1 - refused[0]], want)
+            assert st["resolves"] == 1
+            check_metadata(pool, w, 0, 1, p, 1)
+        else:
+            # the two clusters did not overlap in time: both ran, one after
+            # the other, and the second found every position resident
+            assert not refused and st["resolves"] == 2
+            assert st["misses"] == w.k and st["hits"] == w.k
+
+
 def test_permuted_request_subsets():
     w = _small(n_requests=6, steps=12)
     sel = _random_trace(w, seed=5)

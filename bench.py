@@ -10,13 +10,16 @@ its seeded 256-step selection trace (steps past the end wrap around).
 Passes, each on a freshly reset pool (warm-up steps first, then timed ones):
   graph  -- each step is a CUDA graph of the per-layer hs_resolve launches;
             the L2 is flushed (256 MiB write) before every step and the
-            step itself is timed with CUDA events: ``value``.
+            step itself is timed with CUDA events: ``value``, and, divided
+            by the launches of a step, the resolve kernel's average launch
+            duration inside the graph (``roofline``).
   kernel -- the same steps launched one call at a time with events around
-            every launch: the average resolve-kernel duration (``roofline``).
-  e2e    -- the user's loop through the public API with host buffers:
-            pinned host -> device copy of the step's selections, the
-            resolves, device -> host copy of the published slots, a
-            synchronisation, all inside the timed region (``e2e``).
+            every launch (``roofline.avg_launch_us_eager``, for context).
+  e2e    -- the user's loop through the public API with host buffers: each
+            step a graph of the pinned host -> device copy of its
+            selections, the resolves and the device -> host copy of the
+            published slots, replayed and synchronised, all inside the timed
+            region (``e2e``).
 The host-link ceiling is measured in the same run (pinned H2D memcpy and a
 scattered-record GPU-load probe, best of 10).  The CPU oracle is timed on
 the host's cores over a stated sample (``cpu_baseline``).
@@ -311,12 +314,19 @@ def run_gpu(args, w, rank, world, dist_on):
     total_fetched = reduce_sum(fetched, dist_on, dev)
     del graphs
 
-    # ---- kernel pass (per-launch events) ------------------------------------
+    # the dominant kernel's average launch duration: the graph-timed steps
+    # hold nothing but resolve launches, so a step's events divided by its
+    # launches is the per-launch time inside the decode graph
+    avg_launch_s = dev_s / (K * launches_per_step)
+    link_bytes_per_launch = fetched / (K * launches_per_step)
+    m_per_resolve = misses / resolves
+    hbm_per_launch = R * hbm_bytes_per_resolve(k, B, m_per_resolve, W)
+
+    # ---- kernel pass (per-launch events, eager launches) ---------------------
     pool.reset()
     for s in range(Wm):
         flush.fill_(s)
         step_eager(s % T, main)
-    kst0 = pool.stats()
     kev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             for _ in range(NL)] for _ in range(K)]
     barrier()
@@ -328,27 +338,29 @@ def run_gpu(args, w, rank, world, dist_on):
             hs.hs_resolve(pool.handle, l, R, None, dsel[t, l], k, out[l], None, main)
             kev[i][l][1].record(main)
     barrier()
-    kst1 = pool.stats()
     launch_ms = [a.elapsed_time(b) for row in kev for a, b in row]
-    avg_launch_s = sum(launch_ms) / len(launch_ms) / 1e3
-    k_launches = K * NL
-    k_fetched = kst1["fetched_bytes"] - kst0["fetched_bytes"]
-    k_misses = kst1["misses"] - kst0["misses"]
-    link_bytes_per_launch = k_fetched / k_launches
-    m_per_resolve = k_misses / (k_launches * R)
-    hbm_per_launch = R * hbm_bytes_per_resolve(k, B, m_per_resolve, W)
+    avg_launch_eager_s = sum(launch_ms) / len(launch_ms) / 1e3
 
     # ---- e2e pass (public API, host buffers) ----------------------------------
+    # each step, captured once as a graph like a decode step: pinned host ->
+    # device copy of its selections, the resolves, device -> pinned host copy
+    # of the published slots; every replay is followed by a synchronisation
     pool.reset()
     host_sel = torch.from_numpy(np.ascontiguousarray(sel.transpose(0, 2, 1, 3))).pin_memory()
     host_out = torch.empty((NL, R, k), dtype=torch.int32).pin_memory()
     stage = torch.empty((NL, R, k), dtype=torch.int32, device=dev)
+    e2e_graphs = []
+    for t in range(T):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            stage.copy_(host_sel[t], non_blocking=True)
+            for l in range(NL):
+                hs.hs_resolve(pool.handle, l, R, None, stage[l], k, out[l], None, cap)
+            host_out.copy_(out, non_blocking=True)
+        e2e_graphs.append(g)
 
     def e2e_step(t):
-        stage.copy_(host_sel[t], non_blocking=True)
-        for l in range(NL):
-            hs.hs_resolve(pool.handle, l, R, None, stage[l], k, out[l], None, main)
-        host_out.copy_(out, non_blocking=True)
+        e2e_graphs[t].replay()
         main.synchronize()
 
     for s in range(Wm):
@@ -359,6 +371,7 @@ def run_gpu(args, w, rank, world, dist_on):
         e2e_step((Wm + i) % T)
     barrier()
     e2e_s = reduce_max(time.perf_counter() - e0, dist_on, dev)
+    del e2e_graphs
     pool.close()
 
     peaks = load_peaks()
@@ -418,6 +431,8 @@ def run_gpu(args, w, rank, world, dist_on):
             "peak_source": "pinned cudaMemcpyAsync H2D, 1 GiB, best of 10, this run",
             "algorithmic_bytes_per_launch": link_bytes_per_launch,
             "avg_launch_us": avg_launch_s * 1e6,
+            "avg_launch_from": "graph-timed steps / launches per step",
+            "avg_launch_us_eager": avg_launch_eager_s * 1e6,
         },
         "roofline_hbm": {
             "kernel": "resolve_kernel",
@@ -435,8 +450,9 @@ def run_gpu(args, w, rank, world, dist_on):
             "unit": "resolves/s",
             "h2d_bytes_per_step": NL * R * k * 4,
             "d2h_bytes_per_step": NL * R * k * 4,
-            "what": "pinned H2D of the step's selections, hs_resolve per layer, D2H of the "
-                    "published slots, stream synchronize; wall clock",
+            "what": "per step one graph replay (pinned H2D of the step's selections, "
+                    "hs_resolve per layer, D2H of the published slots) and a stream "
+                    "synchronize; wall clock",
         },
         "gpu_launches": K * launches_per_step,
         "clocks": sampler.summary(),

@@ -186,6 +186,10 @@ cudaError_t launch_prefetch_copy(const DevPool &p, int layer, int n_req, int k,
                                  const void *plan, int sm_count, cudaStream_t st);
 cudaError_t launch_init_lru(uint16_t *lru, int64_t pairs, int B, cudaStream_t st);
 cudaError_t prepare_kernels(size_t max_smem);
+size_t attention_workspace_bytes(int n_req, int k, int heads);
+cudaError_t launch_attention(const void *q, const void *cache, int64_t cache_rows,
+                             const int32_t *idx, int n_req, int k, int heads, float scale,
+                             void *work, float *out, cudaStream_t st);
 cudaError_t launch_gather_probe(const uint8_t *src, uint8_t *dst, const int32_t *idx,
                                 int64_t n_rec, int W, int sm_count, cudaStream_t st);
 

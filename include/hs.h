@@ -219,6 +219,32 @@ int hs_reset(hs_pool *pool);
 int hs_link_probe(size_t bytes, int32_t reps, int32_t record_bytes, double *h2d_gbs,
                   double *gather_gbs);
 
+/*
+ * Sparse attention consumer over published slots (decode).  For each of
+ * n_req requests and each of its `heads` query heads, attention of
+ * q[i][h] (576 bf16) over the k records d_cache[d_idx[i][j]] -- the rows
+ * hs_resolve published -- with keys = the whole 576-element bf16 record and
+ * values = its first 512 elements (MLA latent records, 1152 bytes):
+ *   out[i][h] = softmax_j(scale * q[i][h] . K_j) V_j     (fp32 out[n_req][heads][512]).
+ * This is the attention backend reading the slots resolve publishes; the
+ * model output is unchanged because only the placement of the records
+ * changes (notes, section 5 "Why It Is Exact"; Pith review, "What carries
+ * the argument").  Rows outside [0, cache_rows) are masked out (a request a
+ * resolve rejected publishes -1); a head with no valid key gets zeros.
+ * d_q: device bf16 [n_req][heads][576]; d_cache: a layer's cache,
+ * cache_rows rows of 1152 bytes (hs_device_views); d_idx: device int32
+ * [n_req][k]; d_workspace: hs_attention_workspace_bytes(n_req, k, heads)
+ * bytes of device memory the caller owns (partial results of the key
+ * chunks, overwritten by every call); d_out: device fp32.  All pointers
+ * 16-byte aligned.  heads must be a positive multiple of 16.  Two kernels
+ * are enqueued on `stream`; nothing is allocated.  Errors:
+ * HS_ERR_INVALID_ARG, HS_ERR_CUDA.
+ */
+size_t hs_attention_workspace_bytes(int32_t n_req, int32_t k, int32_t heads);
+int hs_sparse_attention(const void *d_q, const void *d_cache, int64_t cache_rows,
+                        const int32_t *d_idx, int32_t n_req, int32_t k, int32_t heads,
+                        float scale, void *d_workspace, float *d_out, void *stream);
+
 /* Kernels launched per call of hs_resolve / hs_prefetch_plan /
  * hs_prefetch_copy (for launch accounting; always 1 in this build). */
 int32_t hs_kernels_per_call(void);

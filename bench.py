@@ -31,6 +31,7 @@ from __future__ import annotations
 import argparse
 import ctypes
 import json
+import math
 import os
 import statistics
 import sys
@@ -50,7 +51,9 @@ L2_FLUSH_BYTES = 256 << 20
 # Counters of one steady-state resolve launch from an ncu capture (dsa_mla
 # shape, L_ctx cut to 16384: same batch, k, B, W), valid only for the kernel
 # sources they were taken on: reported as null once those sources change.
-PROFILED_SOURCES = {"resolve.cu": "56b273a99f480fdf", "hs_internal.cuh": "505751c1885465e7"}
+# (The header's digest was renewed when attention launcher declarations were
+# added to it; the resolve kernel's code did not change.)
+PROFILED_SOURCES = {"resolve.cu": "56b273a99f480fdf", "hs_internal.cuh": "b3c7ca63be11dd86"}
 PROFILED_LAUNCH = {"dram_bytes": 874_496, "link_bytes": 2_073_600,
                    "algorithmic_link_bytes": 2_073_600}
 
@@ -464,10 +467,12 @@ def run_gpu(args, w, rank, world, dist_on):
 # ------------------------------------------------ exact prefetch overlap ----
 
 def run_prefetch_overlap(args, w):
-    """Exact layer-wise prefetch against stand-in compute.
+    """Exact layer-wise prefetch against compute.
 
-    Each layer of a decode step is its resolve followed by a bf16 GEMM that
-    stands in for the layer's attention and MLP (`--compute-us` long).  For
+    Each layer of a decode step is its resolve, the sparse attention
+    consumer over the slots it published (`--attn-heads` query heads per
+    request), and a bf16 GEMM that stands in for the layer's MLP
+    (`--compute-us` long).  For
     a layer that shares its anchor's selection, prefetch ON plans its misses
     right after the anchor's resolve and copies them on a side stream, so the
     copy overlaps the compute of the layers in between; its own resolve then
@@ -489,13 +494,31 @@ def run_prefetch_overlap(args, w):
     for r in range(R):
         for l in range(NL):
             records.fill(pool.host_records(r, l).ctypes.data, w, r, l)
-    out = torch.empty((NL, R, k), dtype=torch.int32, device=dev)
+    # published slots; before the first resolve, k distinct rows per request
+    B = w.slots
+    out = (torch.arange(R, dtype=torch.int32, device=dev)[:, None] * B
+           + torch.arange(k, dtype=torch.int32, device=dev)[None, :]).repeat(NL, 1, 1)
     plans = {l: torch.empty(hs.hs_plan_bytes(R, k), dtype=torch.uint8, device=dev)
              for l in range(NL) if w.anchors[l] != l}
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
     main, side = torch.cuda.current_stream(), torch.cuda.Stream()
 
-    # stand-in compute: [4096 x 4096] x [4096 x n] bf16, n chosen for the target time
+    heads = args.attn_heads
+    attn = w.record_bytes == 1152 and heads > 0
+    if attn:
+        q = torch.randn((R, heads, 576), device=dev).to(torch.bfloat16)
+        ws = torch.empty(hs.hs_attention_workspace_bytes(R, k, heads), dtype=torch.uint8,
+                         device=dev)
+        o = torch.empty((R, heads, 512), dtype=torch.float32, device=dev)
+        caches = [pool.views(l)["cache"] for l in range(NL)]
+        scale = 1.0 / math.sqrt(576.0)
+
+    def attention(l):
+        if attn:
+            hs.hs_sparse_attention(q, caches[l], R * B, out[l], R, k, heads, scale, ws, o,
+                                   stream=main)
+
+    # MLP stand-in: [4096 x 4096] x [4096 x n] bf16, n chosen for the target time
     a = torch.randn(4096, 4096, device=dev, dtype=torch.bfloat16)
     b = torch.randn(4096, 4096, device=dev, dtype=torch.bfloat16)
     for _ in range(3):
@@ -536,6 +559,7 @@ def run_prefetch_overlap(args, w):
                     pool.resolve(l, dsel[t, l], out[l], plan=plans[l], stream=main)
                 else:
                     pool.resolve(l, dsel[t, l], out[l], stream=main)
+            attention(l)
             compute()
 
     results = {}
@@ -559,6 +583,8 @@ def run_prefetch_overlap(args, w):
             results[mode + "_stats"] = {x: st[x] for x in ("misses", "fetched_bytes",
                                                           "prefetched_bytes", "plan_hits",
                                                           "plan_mismatches", "status")}
+    attn_res = time_attention(lambda: attention(0), flush, main, R, k, heads,
+                              args.steps) if attn else None
     pool.close()
     hidden = 1.0 - (results["on"] - results["compute"]) / (results["off"] - results["compute"])
     shared = sum(1 for l in range(NL) if w.anchors[l] != l)
@@ -567,13 +593,55 @@ def run_prefetch_overlap(args, w):
         "value": hidden, "unit": "fraction of resolve time hidden",
         "higher_is_better": True,
         "config": {"workload": workload_name(w), "shared_layers_per_step": shared,
-                   "compute_stand_in": f"bf16 GEMM 4096x4096x{n} after every layer",
+                   "attention": (f"hs_sparse_attention over the published slots, {heads} "
+                                 f"heads per request" if attn else "none"),
+                   "mlp_stand_in": f"bf16 GEMM 4096x4096x{n} after every layer",
                    "l2": "flushed before every timed step"},
         "ms_per_step": {"compute_only": results["compute"], "prefetch_off": results["off"],
                         "prefetch_on": results["on"]},
         "counters": {"off": results["off_stats"], "on": results["on_stats"]},
+        "attention": attn_res,
         "steps": args.steps, "warmup": args.warmup,
     }
+
+
+def attention_bytes(R: int, k: int, heads: int) -> int:
+    """Algorithmic HBM bytes of one sparse attention call: the k gathered
+    576-element bf16 records and k int32 slot indices per request, the bf16
+    queries, the fp32 outputs.  The flash-decoding partials (written by one
+    kernel, read by the next, L2-resident at these sizes) are implementation
+    traffic and not counted."""
+    return R * k * (1152 + 4) + R * heads * (1152 + 512 * 4)
+
+
+def time_attention(call, flush, stream, R, k, heads, steps):
+    """CUDA-event time of one sparse attention call (both of its kernels) on
+    `stream`, L2 flushed before every timed call; HBM roofline against the
+    measured copy bandwidth."""
+    import torch
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    total = 0.0
+    for i in range(steps):
+        flush.fill_(i)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        total += e0.elapsed_time(e1)
+    s = total / steps / 1e3
+    nbytes = attention_bytes(R, k, heads)
+    peaks = load_peaks()
+    peak = peaks.get("hbm_gbs") if peaks else None
+    achieved = nbytes / s / 1e9
+    return {"us_per_call": s * 1e6, "kernels_per_call": 2,
+            "algorithmic_bytes_per_call": nbytes,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak if peak else None,
+                         "peak_source": ("MEASURED_PEAKS.json hbm_gbs (of measured)"
+                                         if peak else None)}}
 
 
 # ------------------------------------------------------------------ main ----
@@ -596,7 +664,10 @@ def main(argv=None):
                     help="measure exact layer-wise prefetch against stand-in compute "
                          "(a workload with shared layers, e.g. tight_prefetch)")
     ap.add_argument("--compute-us", type=float, default=60.0,
-                    help="stand-in compute per layer for --prefetch-overlap")
+                    help="MLP stand-in compute per layer for --prefetch-overlap")
+    ap.add_argument("--attn-heads", type=int, default=16,
+                    help="query heads per request of the sparse attention consumer in "
+                         "--prefetch-overlap (a multiple of 16; 0: no attention)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -9,7 +9,8 @@ its seeded 256-step selection trace (steps past the end wrap around).
 
 Passes, each on a freshly reset pool (warm-up steps first, then timed ones):
   graph  -- each step is a CUDA graph of the per-layer hs_resolve launches;
-            the L2 is flushed (256 MiB write) before every step and the
+            the L2 is flushed (a 256 MiB write, then a 256 MiB read so
+            that no dirty line is left to write back) before every step and the
             step itself is timed with CUDA events: ``value``, and, divided
             by the launches of a step, the resolve kernel's average launch
             duration inside the graph (``roofline``).
@@ -69,6 +70,22 @@ def profiled_counters():
 
 
 # ---------------------------------------------------------------- helpers ---
+
+class L2Flush:
+    """Empties the L2 between timed iterations: a 256 MiB write (twice the
+    126 MB L2), then a 256 MiB read of a second buffer, so that the L2 holds
+    only clean lines and the timed work pays no write-back of the flush."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+        self.r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+        self.sink = None
+
+    def __call__(self, i):
+        self.w.fill_(i)
+        self.sink = self.r.max()
+
 
 def workload_name(w) -> str:
     return (f"{w.name}: batch {w.n_requests}, {w.n_layers} sparse layers, "
@@ -262,7 +279,7 @@ def run_gpu(args, w, rank, world, dist_on):
         for l in range(NL):
             records.fill(pool.host_records(r, l).ctypes.data, w, r, l)
     out = torch.empty((NL, R, k), dtype=torch.int32, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    flush = L2Flush(dev)
     main = torch.cuda.current_stream()
     Wm, K = args.warmup, args.steps
     launches_per_step = NL * hs.hs_kernels_per_call()
@@ -288,7 +305,7 @@ def run_gpu(args, w, rank, world, dist_on):
                 hs.hs_resolve(pool.handle, l, R, None, dsel[t, l], k, out[l], None, cap)
         graphs.append(g)
     for s in range(Wm):
-        flush.fill_(s)
+        flush(s)
         graphs[s % T].replay()
     st0 = pool.stats()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -298,7 +315,7 @@ def run_gpu(args, w, rank, world, dist_on):
     sampler.start()
     wall0 = time.perf_counter()
     for i in range(K):
-        flush.fill_(i)
+        flush(i)
         ev[i][0].record(main)
         graphs[(Wm + i) % T].replay()
         ev[i][1].record(main)
@@ -328,13 +345,13 @@ def run_gpu(args, w, rank, world, dist_on):
     # ---- kernel pass (per-launch events, eager launches) ---------------------
     pool.reset()
     for s in range(Wm):
-        flush.fill_(s)
+        flush(s)
         step_eager(s % T, main)
     kev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             for _ in range(NL)] for _ in range(K)]
     barrier()
     for i in range(K):
-        flush.fill_(i)
+        flush(i)
         t = (Wm + i) % T
         for l in range(NL):
             kev[i][l][0].record(main)
@@ -402,7 +419,7 @@ def run_gpu(args, w, rank, world, dist_on):
             "resolves_per_step": R * NL * world,
             "parallelism": f"requests sharded, {world} independent pool(s), no collective",
             "launch": f"per-step CUDA graph of {NL} hs_resolve launches",
-            "l2": "flushed before every timed step (256 MiB write, outside the events)",
+            "l2": "flushed before every timed step (256 MiB write + 256 MiB read, outside the events)",
             "record_values": "bf16 N(0,1)" if w.value_format else "fp16 U(-1,1)",
         },
         "miss_fetch": {
@@ -500,22 +517,20 @@ def run_prefetch_overlap(args, w):
            + torch.arange(k, dtype=torch.int32, device=dev)[None, :]).repeat(NL, 1, 1)
     plans = {l: torch.empty(hs.hs_plan_bytes(R, k), dtype=torch.uint8, device=dev)
              for l in range(NL) if w.anchors[l] != l}
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    flush = L2Flush(dev)
     main, side = torch.cuda.current_stream(), torch.cuda.Stream()
 
     heads = args.attn_heads
     attn = w.record_bytes == 1152 and heads > 0
     if attn:
         q = torch.randn((R, heads, 576), device=dev).to(torch.bfloat16)
-        ws = torch.empty(hs.hs_attention_workspace_bytes(R, k, heads), dtype=torch.uint8,
-                         device=dev)
         o = torch.empty((R, heads, 512), dtype=torch.float32, device=dev)
         caches = [pool.views(l)["cache"] for l in range(NL)]
         scale = 1.0 / math.sqrt(576.0)
 
     def attention(l):
         if attn:
-            hs.hs_sparse_attention(q, caches[l], R * B, out[l], R, k, heads, scale, ws, o,
+            hs.hs_sparse_attention(q, caches[l], R * B, out[l], R, k, heads, scale, o,
                                    stream=main)
 
     # MLP stand-in: [4096 x 4096] x [4096 x n] bf16, n chosen for the target time
@@ -570,7 +585,7 @@ def run_prefetch_overlap(args, w):
         torch.cuda.synchronize()
         total = 0.0
         for i in range(args.steps):
-            flush.fill_(i)
+            flush(i)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(main)
             step((args.warmup + i) % T, mode)
@@ -608,9 +623,7 @@ def run_prefetch_overlap(args, w):
 def attention_bytes(R: int, k: int, heads: int) -> int:
     """Algorithmic HBM bytes of one sparse attention call: the k gathered
     576-element bf16 records and k int32 slot indices per request, the bf16
-    queries, the fp32 outputs.  The flash-decoding partials (written by one
-    kernel, read by the next, L2-resident at these sizes) are implementation
-    traffic and not counted."""
+    queries, the fp32 outputs (the split results merge on chip)."""
     return R * k * (1152 + 4) + R * heads * (1152 + 512 * 4)
 
 
@@ -624,7 +637,7 @@ def time_attention(call, flush, stream, R, k, heads, steps):
     torch.cuda.synchronize()
     total = 0.0
     for i in range(steps):
-        flush.fill_(i)
+        flush(i)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         call()
@@ -636,12 +649,55 @@ def time_attention(call, flush, stream, R, k, heads, steps):
     peaks = load_peaks()
     peak = peaks.get("hbm_gbs") if peaks else None
     achieved = nbytes / s / 1e9
-    return {"us_per_call": s * 1e6, "kernels_per_call": 2,
+    return {"us_per_call": s * 1e6, "kernels_per_call": 1,
             "algorithmic_bytes_per_call": nbytes,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak if peak else None,
                          "peak_source": ("MEASURED_PEAKS.json hbm_gbs (of measured)"
                                          if peak else None)}}
+
+
+# ------------------------------------------------ attention consumer alone ----
+
+def run_attention(args, w):
+    """The sparse attention consumer alone on a workload's shape: a layer
+    cache of R*B random bf16 records in HBM, k distinct published rows per
+    request inside its own B slots (as a resolve publishes them), `--attn-heads`
+    query heads per request; L2 flushed before every timed call."""
+    import torch
+
+    from hierarchical_kv_cache_resolve_gb300 import hs
+    if w.record_bytes != 1152:
+        raise SystemExit("bench.py --attention: the consumer reads 576-element MLA records")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    R, k, B, heads = w.n_requests, w.k, w.slots, args.attn_heads
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed)
+    cache = torch.randn((R * B, 576), device=dev, generator=g).to(torch.bfloat16)
+    idx = torch.stack([torch.randperm(B, device=dev, generator=g)[:k] + r * B
+                       for r in range(R)]).to(torch.int32)
+    q = torch.randn((R, heads, 576), device=dev, generator=g).to(torch.bfloat16)
+    o = torch.empty((R, heads, 512), dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
+    main = torch.cuda.current_stream()
+    scale = 1.0 / math.sqrt(576.0)
+
+    def call():
+        hs.hs_sparse_attention(q, cache, R * B, idx, R, k, heads, scale, o, stream=main)
+
+    props = torch.cuda.get_device_properties(dev)
+    sampler = ClockSampler(f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:"
+                           f"{props.pci_device_id:02x}.0")
+    sampler.start()
+    res = time_attention(call, flush, main, R, k, heads, args.steps)
+    sampler.stop()
+    status = hs.hs_attention_status()
+    return {"metric": "sparse attention over published slots: gathered HBM GB/s",
+            "value": res["roofline"]["achieved"], "unit": "GB/s", "higher_is_better": True,
+            "config": {"workload": workload_name(w), "heads": heads,
+                       "l2": "flushed before every timed call"},
+            "attention": res, "status": status, "clocks": sampler.summary(),
+            "steps": args.steps, "warmup": 3}
 
 
 # ------------------------------------------------------------------ main ----
@@ -665,6 +721,8 @@ def main(argv=None):
                          "(a workload with shared layers, e.g. tight_prefetch)")
     ap.add_argument("--compute-us", type=float, default=60.0,
                     help="MLP stand-in compute per layer for --prefetch-overlap")
+    ap.add_argument("--attention", action="store_true",
+                    help="time the sparse attention consumer alone on the workload's shape")
     ap.add_argument("--attn-heads", type=int, default=16,
                     help="query heads per request of the sparse attention consumer in "
                          "--prefetch-overlap (a multiple of 16; 0: no attention)")
@@ -717,9 +775,10 @@ def main(argv=None):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     w = rank_workload(base, rank)
-    if args.prefetch_overlap:
+    if args.prefetch_overlap or args.attention:
         if rank == 0:
-            print(json.dumps(run_prefetch_overlap(args, w)))
+            run = run_prefetch_overlap if args.prefetch_overlap else run_attention
+            print(json.dumps(run(args, w)))
         return 0
     res = run_gpu(args, w, rank, world, dist_on)
     if rank == 0:

@@ -126,7 +126,8 @@ class LayerState(ctypes.Structure):
 EXPORTS = ("hs_create_pool", "hs_destroy_pool", "hs_host_records", "hs_device_views",
            "hs_resolve", "hs_plan_bytes", "hs_prefetch_plan", "hs_prefetch_copy",
            "hs_stats", "hs_reset", "hs_link_probe", "hs_kernels_per_call", "hs_strerror",
-           "hs_resolve_noalloc", "hs_attention_workspace_bytes", "hs_sparse_attention")
+           "hs_resolve_noalloc", "hs_sparse_attention",
+           "hs_attention_status")
 
 
 def _declare(lib):
@@ -149,9 +150,9 @@ def _declare(lib):
         "hs_strerror": ([ctypes.c_int], ctypes.c_char_p),
         "hs_resolve_noalloc": ([ctypes.POINTER(LayerState), i32, vp, vp, i32, vp, vp, vp],
                                ctypes.c_int),
-        "hs_attention_workspace_bytes": ([i32, i32, i32], ctypes.c_size_t),
-        "hs_sparse_attention": ([vp, vp, i64, vp, i32, i32, i32, ctypes.c_float, vp, vp, vp],
+        "hs_sparse_attention": ([vp, vp, i64, vp, i32, i32, i32, ctypes.c_float, vp, vp],
                                 ctypes.c_int),
+        "hs_attention_status": ([ctypes.POINTER(ctypes.c_uint32)], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)

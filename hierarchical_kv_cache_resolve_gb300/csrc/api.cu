@@ -283,24 +283,24 @@ int hs_reset(hs_pool *pool) {
     return reset_state(pool);
 }
 
-size_t hs_attention_workspace_bytes(int32_t n_req, int32_t k, int32_t heads) {
-    if (n_req < 0 || k < 1 || heads < 1) return 0;
-    return hs::attention_workspace_bytes(n_req, k, heads);
-}
-
 int hs_sparse_attention(const void *d_q, const void *d_cache, int64_t cache_rows,
                         const int32_t *d_idx, int32_t n_req, int32_t k, int32_t heads,
-                        float scale, void *d_workspace, float *d_out, void *stream) {
+                        float scale, float *d_out, void *stream) {
     auto misaligned = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
-    if (!d_q || !d_cache || !d_idx || !d_workspace || !d_out || cache_rows < 1 || n_req < 0 ||
-        n_req > 65535 || k < 1 || heads < 16 || heads % 16 != 0 || heads / 16 > 65535 ||
-        misaligned(d_q) || misaligned(d_cache) || misaligned(d_workspace) || misaligned(d_out))
+    if (!d_q || !d_cache || !d_idx || !d_out || cache_rows < 1 || n_req < 0 || n_req > 65535 ||
+        k < 1 || heads < 16 || heads % 16 != 0 || heads / 16 > 65535 || misaligned(d_q) ||
+        misaligned(d_cache) || misaligned(d_out))
         return HS_ERR_INVALID_ARG;
     if (n_req == 0) return HS_OK;
     const cudaError_t e = hs::launch_attention(d_q, d_cache, cache_rows, d_idx, n_req, k, heads,
-                                               scale, d_workspace, d_out,
-                                               static_cast<cudaStream_t>(stream));
+                                               scale, d_out, static_cast<cudaStream_t>(stream));
     return cuda_ok(e) ? HS_OK : HS_ERR_CUDA;
+}
+
+int hs_attention_status(uint32_t *status) {
+    if (!status) return HS_ERR_INVALID_ARG;
+    if (!cuda_ok(cudaDeviceSynchronize())) return HS_ERR_CUDA;
+    return cuda_ok(hs::attention_status(status)) ? HS_OK : HS_ERR_CUDA;
 }
 
 int hs_link_probe(size_t bytes, int32_t reps, int32_t record_bytes, double *h2d_gbs,

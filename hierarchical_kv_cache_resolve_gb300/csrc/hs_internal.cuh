@@ -131,12 +131,13 @@ __host__ __device__ inline SmemLayout smem_layout(int B, int k, bool with_plan, 
 
 // A follower CTA of a resolve cluster needs none of the leader's arrays.
 // After the 256-byte header it keeps: the share entries each warp staged
-// (kStageMax per warp), one staged-bit word per block of 32 share entries,
+// and their positions (kStageMax per warp each), one staged-bit word per
+// block of 32 share entries,
 // the list (positions, slots) of misses it did not stage, and then the
 // staging area for whole records, `cap` records per warp.
 constexpr int kStageMax = 32;
 struct FollowerLayout {
-    uint32_t stg, sbits, xp, xs, stage;
+    uint32_t stg, stgpos, sbits, xp, xs, stage;
     int cap;
 };
 
@@ -144,6 +145,7 @@ __host__ __device__ inline FollowerLayout follower_lists(int k) {
     FollowerLayout f;
     uint32_t o = 256;
     f.stg = o;   o += 4u * kWarps * kStageMax;
+    f.stgpos = o; o += 4u * kWarps * kStageMax;
     f.sbits = o; o += align16(4u * (uint32_t)((k + 31) / 32));
     f.xp = o;    o += align16(4u * (uint32_t)k);
     f.xs = o;    o += align16(4u * (uint32_t)k);
@@ -186,10 +188,10 @@ cudaError_t launch_prefetch_copy(const DevPool &p, int layer, int n_req, int k,
                                  const void *plan, int sm_count, cudaStream_t st);
 cudaError_t launch_init_lru(uint16_t *lru, int64_t pairs, int B, cudaStream_t st);
 cudaError_t prepare_kernels(size_t max_smem);
-size_t attention_workspace_bytes(int n_req, int k, int heads);
 cudaError_t launch_attention(const void *q, const void *cache, int64_t cache_rows,
                              const int32_t *idx, int n_req, int k, int heads, float scale,
-                             void *work, float *out, cudaStream_t st);
+                             float *out, cudaStream_t st);
+cudaError_t attention_status(uint32_t *status);
 cudaError_t launch_gather_probe(const uint8_t *src, uint8_t *dst, const int32_t *idx,
                                 int64_t n_rec, int W, int sm_count, cudaStream_t st);
 

@@ -153,6 +153,16 @@ __device__ __forceinline__ void bulk_wait_read() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// Acquire load / release store of a u32 in global memory at GPU scope.
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *a) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu(uint32_t *a, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
+
 // Programmatic dependent launch: wait for the grids this one depends on to
 // complete (and their writes to be visible), then let the next grid in the
 // stream start launching.  Both are no-ops without the launch attribute.
@@ -284,15 +294,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int32_t *selr = sel_g + (int64_t)ireq * k;
 
     if (tid < H_SUMS) hdr[tid] = 0u;
-    // everything above touched only registers and shared memory; global
-    // inputs may be written by the previous grid in the stream
-    grid_dependency_wait();
+    // Everything above touched only registers and shared memory.  Global
+    // inputs may be written by the previous grid in the stream: a plan
+    // resolve and a plan waits for it here.  A plain resolve starts before
+    // it completes (programmatic launch) and acts only on what it has
+    // checked after the wait: the leader decides on the pair's metadata and
+    // keeps the decision only if the pair's resolve counter (read before
+    // the metadata, moved after every commit), the request id and the
+    // selection are unchanged once the previous grid has completed, and
+    // decides again otherwise; the followers stage the records they predict
+    // to miss and check each one against the leader's selection.  Nothing
+    // is written to global memory before the wait, so a launch that
+    // overlaps the previous one stays exact.
+    const bool early = !kPlanOnly && !with_plan;
+    if (!early) grid_dependency_wait();
     allow_dependent_launch();
     if (crank == 0) copy_to_smem(sel_s, selr, 4 * k);  // independent of the request id
 
-    const int r = req_ids ? req_ids[ireq] : ireq;
-    const bool r_ok = r >= 0 && r < p.R;
-    const int64_t pair = (int64_t)layer * p.R + (r_ok ? r : 0);
+    int r = req_ids ? req_ids[ireq] : ireq;
+    bool r_ok = r >= 0 && r < p.R;
+    int64_t pair = (int64_t)layer * p.R + (r_ok ? r : 0);
     const uint8_t *host_pair = p.host + ((int64_t)(r_ok ? r : 0) * p.NL + layer) * p.L * W;
     uint8_t *cache_pair = p.cache + pair * B * (int64_t)W;
 
@@ -300,259 +321,297 @@ __global__ void __launch_bounds__(kThreads, 1)
     int staged_n = 0;
 
     if (crank == 0) {
-        // ---------------- P0: load -------------------------------------
-        bool took_busy = false;
-        if (r_ok) {
-            copy_to_smem(spos_s, p.slot_pos + pair * B, 4 * B);
-            copy_to_smem(order_s, p.lru + pair * B, 2 * B);
-        }
-        {
-            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-            uint4 *kz = reinterpret_cast<uint4 *>(keys);
-            for (int i = tid; i < H / 4; i += kThreads) kz[i] = z;
-            uint4 *bz = reinterpret_cast<uint4 *>(bitmap);
-            for (int i = tid; i < sl.M / 128; i += kThreads) bz[i] = z;
-        }
-        uint32_t a0 = 0, t0 = 0;
-        if (tid == 0) {
-            if (!r_ok) {
-                a0 |= HS_STATUS_REQ_RANGE;
-            } else if (!kPlanOnly) {
-                if (atomicCAS(&p.busy[pair], 0u, 1u) == 0u)
-                    took_busy = true;
-                else
-                    a0 |= HS_STATUS_REQ_BUSY;
-            }
-            t0 = r_ok ? p.tcount[pair] + 1u : 0u;
-        }
-        cp_async_wait_all();
-        __syncthreads();  // header zeroed, shared copies landed
-
-        // ---------------- P1: validate, hash build, membership bits ------
-        {
-            uint32_t bad = 0;
+        bool took_busy = false;  // (thread 0)
+        uint32_t t_seen = 0;     // (thread 0) the pair's resolve counter as read
+        for (int attempt = 0;; ++attempt) {
+            const bool speculative = early && attempt == 0;
+            // ---------------- P0: load -------------------------------------
+            uint32_t a0 = 0, t0 = 0;
             if (tid == 0) {
-                bad = a0;
-                hdr[H_T] = t0;
+                hdr[H_ABORT] = 0u;
+                if (!r_ok) {
+                    a0 |= HS_STATUS_REQ_RANGE;
+                } else {
+                    if (!kPlanOnly && !speculative && !took_busy) {
+                        if (atomicCAS(&p.busy[pair], 0u, 1u) == 0u)
+                            took_busy = true;
+                        else
+                            a0 |= HS_STATUS_REQ_BUSY;
+                    }
+                    // before the metadata copies below: a commit they might see
+                    // in part moves the counter
+                    t_seen = ld_acquire_gpu(&p.tcount[pair]);
+                    t0 = t_seen + 1u;
+                }
             }
+            if (attempt > 0) copy_to_smem(sel_s, selr, 4 * k);
+            __syncthreads();
             if (r_ok) {
-                for (int i = tid; i < k; i += kThreads) {
-                    const int32_t v = sel_s[i];
-                    hit_s[i] = -1;
-                    if (v < 0 || (int64_t)v >= p.L) {
-                        bad |= HS_STATUS_POS_RANGE;
-                        continue;
-                    }
-                    const uint32_t mb = member_bit(v, exact_bits, mshift);
-                    atomicOr(&bitmap[mb >> 5], 1u << (mb & 31));
-                    uint32_t h = hash_slot(v, hshift);
-                    for (int probe = 0; probe < H; ++probe) {
-                        const uint32_t old = atomicCAS(&keys[h], 0u, (uint32_t)v + 1u);
-                        if (old == 0u) {
-                            kidx[h] = (uint16_t)i;
-                            break;
-                        }
-                        if (old == (uint32_t)v + 1u) {
-                            bad |= HS_STATUS_POS_DUP;
-                            break;
-                        }
-                        h = (h + 1) & (uint32_t)(H - 1);
-                    }
-                }
-                for (int b = tid; b < B; b += kThreads) {
-                    const int32_t v = spos_s[b];
-                    flags_s[b] = 0;
-                    if (v < -1 || (int64_t)v >= p.L || order_s[b] >= (uint16_t)B)
-                        bad |= HS_STATUS_META;
-                }
+                copy_to_smem(spos_s, p.slot_pos + pair * B, 4 * B);
+                copy_to_smem(order_s, p.lru + pair * B, 2 * B);
             }
-            if (bad) atomicOr(&hdr[H_ABORT], bad);
-        }
-        __syncthreads();
-        const uint32_t abort_bits = hdr[H_ABORT];
+            {
+                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                uint4 *kz = reinterpret_cast<uint4 *>(keys);
+                for (int i = tid; i < H / 4; i += kThreads) kz[i] = z;
+                uint4 *bz = reinterpret_cast<uint4 *>(bitmap);
+                for (int i = tid; i < sl.M / 128; i += kThreads) bz[i] = z;
+            }
+            cp_async_wait_all();
+            __syncthreads();  // header set, shared copies landed
 
-        if (abort_bits == 0u) {
-            // ------------- P2: probe the slots --------------------------
-            // a slot whose position has no membership bit is not selected;
-            // the others look their position up in the hash table
-            for (int b0 = tid; b0 < B; b0 += kThreads * 4) {
-                int32_t pv[4];
-                uint32_t in[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int b = b0 + u * kThreads;
-                    pv[u] = b < B ? spos_s[b] : -1;
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    in[u] = 0u;
-                    if (pv[u] >= 0) {
-                        const uint32_t mb = member_bit(pv[u], exact_bits, mshift);
-                        in[u] = (bitmap[mb >> 5] >> (mb & 31)) & 1u;
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    if (!in[u]) continue;
-                    const int32_t pos = pv[u];
-                    uint32_t h = hash_slot(pos, hshift);
-                    for (int probe = 0; probe < H; ++probe) {
-                        const uint32_t key = keys[h];
-                        if (key == 0u) break;
-                        if (key == (uint32_t)pos + 1u) {
-                            hit_s[kidx[h]] = b0 + u * kThreads;
-                            flags_s[b0 + u * kThreads] = 1;
-                            break;
-                        }
-                        h = (h + 1) & (uint32_t)(H - 1);
-                    }
-                }
-            }
-            __syncthreads();
-
-            // ------------- P3: misses and victims (ballot scans) --------
-            // warp w owns a contiguous block of 32*seg elements of each
-            // array; element order = warp, then round, then lane.  Loads of
-            // up to 8 rounds are issued before their ballots.
-            const int segK = (k + kThreads - 1) / kThreads;
-            const int segB = (B + kThreads - 1) / kThreads;
-            const int baseK = warp * 32 * segK, baseB = warp * 32 * segB;
-            const uint32_t lt = lanemask_lt();
-            uint32_t cm = 0, cn = 0;
-            for (int s0 = 0; s0 < segK; s0 += 8) {
-                bool pr[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int i = baseK + (s0 + u) * 32 + lane;
-                    pr[u] = s0 + u < segK && i < k && hit_s[i] < 0;
-                }
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    if (s0 + u < segK) cm += __popc(__ballot_sync(0xFFFFFFFFu, pr[u]));
-            }
-            for (int s0 = 0; s0 < segB; s0 += 8) {
-                int ob[8];
-                bool pr[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int q = baseB + (s0 + u) * 32 + lane;
-                    ob[u] = (s0 + u < segB && q < B) ? (int)order_s[q] : -1;
-                }
-#pragma unroll
-                for (int u = 0; u < 8; ++u) pr[u] = ob[u] >= 0 && !(flags_s[ob[u]] & 1);
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    if (s0 + u < segB) cn += __popc(__ballot_sync(0xFFFFFFFFu, pr[u]));
-            }
-            uint32_t total;
-            const uint32_t base = warp_counts_exscan(cm | (cn << 16), sums, &total);
-            const int m = (int)(total & 0xFFFFu);
-            const int nh = (int)(total >> 16);
-            uint32_t mr = base & 0xFFFFu, nr = base >> 16;
-            for (int s0 = 0; s0 < segK; s0 += 8) {
-                bool pr[8];
-                int32_t sv[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int i = baseK + (s0 + u) * 32 + lane;
-                    pr[u] = s0 + u < segK && i < k && hit_s[i] < 0;
-                    sv[u] = pr[u] ? sel_s[i] : 0;
-                }
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    if (s0 + u >= segK) break;
-                    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, pr[u]);
-                    if (pr[u]) {
-                        const uint32_t rank = mr + __popc(bal & lt);
-                        mpos[rank] = sv[u];
-                        hit_s[baseK + (s0 + u) * 32 + lane] = -2 - (int32_t)rank;
-                    }
-                    mr += __popc(bal);
-                }
-            }
-            for (int s0 = 0; s0 < segB; s0 += 8) {
-                int ob[8];
-                bool pr[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int q = baseB + (s0 + u) * 32 + lane;
-                    ob[u] = (s0 + u < segB && q < B) ? (int)order_s[q] : -1;
-                }
-#pragma unroll
-                for (int u = 0; u < 8; ++u) pr[u] = ob[u] >= 0 && !(flags_s[ob[u]] & 1);
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    if (s0 + u >= segB) break;
-                    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, pr[u]);
-                    if (pr[u]) {
-                        const uint32_t rank = nr + __popc(bal & lt);
-                        const int b = ob[u];
-                        if ((int)rank < m) {
-                            mslot[rank] = b;
-                            flags_s[b] |= 2;
-                            if (with_plan) vrank_s[b] = (uint16_t)rank;
-                        } else {
-                            neworder[rank - m] = (uint16_t)b;
-                        }
-                    }
-                    nr += __popc(bal);
-                }
-            }
-            if (tid == 0) {
-                hdr[H_M] = (uint32_t)m;
-                hdr[H_NH] = (uint32_t)nh;
-                hdr[H_F] = (uint32_t)m;
-                hdr[H_FLIST] = 0u;
-            }
-            __syncthreads();
-
-            // ------------- P3b: consume a plan --------------------------
-            if (with_plan) {
-                const PlanHeader *ph = reinterpret_cast<const PlanHeader *>(plan_in);
-                const int32_t *eh =
-                    reinterpret_cast<const int32_t *>(plan_in + 16 + (size_t)ireq * plan_entry_bytes(k));
-                const bool ok = ph->magic == kPlanMagic && ph->n_req == n_req && ph->k == k &&
-                                ph->layer == layer && eh[0] >= 0 && eh[0] <= k && eh[1] == r;
-                const int mp = ok ? eh[0] : 0;
-                if (!ok && tid == 0) atomicOr(p.status, HS_STATUS_PLAN);
-                const int32_t *ppos = eh + 4;
-                const int32_t *pslot = ppos + k;
-                const int n = m > mp ? m : mp;
-                for (int j = tid; j < n; j += kThreads) {
-                    const int32_t pp = j < mp ? ppos[j] : -1;
-                    const int32_t ps = j < mp ? pslot[j] : -1;
-                    if (j < m && j < mp && pp == mpos[j] && ps == mslot[j]) {
-                        atomicAdd(&hdr[H_PHIT], 1u);
-                        continue;
-                    }
-                    atomicAdd(&hdr[H_PMISS], 1u);
-                    if (j < m) {
-                        const uint32_t f = atomicAdd(&hdr[H_NF], 1u);
-                        fpos[f] = mpos[j];
-                        fslot[f] = mslot[j];
-                    }
-                    if (j < mp) {
-                        if (ps >= 0 && ps < B && pp >= 0 && (int64_t)pp < p.L) {
-                            // the copy wrote slot ps: refill it with its owner
-                            const int32_t owner = (flags_s[ps] & 2) ? mpos[vrank_s[ps]] : spos_s[ps];
-                            if (owner >= 0) {
-                                const uint32_t f = atomicAdd(&hdr[H_NF], 1u);
-                                fpos[f] = owner;
-                                fslot[f] = ps;
-                            }
-                        } else {
-                            atomicOr(p.status, HS_STATUS_PLAN);
-                        }
-                    }
-                }
-                __syncthreads();
+            // ---------------- P1: validate, hash build, membership bits ------
+            {
+                uint32_t bad = 0;
                 if (tid == 0) {
-                    hdr[H_F] = hdr[H_NF];
-                    hdr[H_FLIST] = 1u;
+                    bad = a0;
+                    hdr[H_T] = t0;
+                }
+                if (r_ok) {
+                    for (int i = tid; i < k; i += kThreads) {
+                        const int32_t v = sel_s[i];
+                        hit_s[i] = -1;
+                        if (v < 0 || (int64_t)v >= p.L) {
+                            bad |= HS_STATUS_POS_RANGE;
+                            continue;
+                        }
+                        const uint32_t mb = member_bit(v, exact_bits, mshift);
+                        atomicOr(&bitmap[mb >> 5], 1u << (mb & 31));
+                        uint32_t h = hash_slot(v, hshift);
+                        for (int probe = 0; probe < H; ++probe) {
+                            const uint32_t old = atomicCAS(&keys[h], 0u, (uint32_t)v + 1u);
+                            if (old == 0u) {
+                                kidx[h] = (uint16_t)i;
+                                break;
+                            }
+                            if (old == (uint32_t)v + 1u) {
+                                bad |= HS_STATUS_POS_DUP;
+                                break;
+                            }
+                            h = (h + 1) & (uint32_t)(H - 1);
+                        }
+                    }
+                    for (int b = tid; b < B; b += kThreads) {
+                        const int32_t v = spos_s[b];
+                        flags_s[b] = 0;
+                        if (v < -1 || (int64_t)v >= p.L || order_s[b] >= (uint16_t)B)
+                            bad |= HS_STATUS_META;
+                    }
+                }
+                if (bad) atomicOr(&hdr[H_ABORT], bad);
+            }
+            __syncthreads();
+
+            if (hdr[H_ABORT] == 0u) {
+                // ------------- P2: probe the slots --------------------------
+                // a slot whose position has no membership bit is not selected;
+                // the others look their position up in the hash table
+                for (int b0 = tid; b0 < B; b0 += kThreads * 4) {
+                    int32_t pv[4];
+                    uint32_t in[4];
+    #pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int b = b0 + u * kThreads;
+                        pv[u] = b < B ? spos_s[b] : -1;
+                    }
+    #pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        in[u] = 0u;
+                        if (pv[u] >= 0) {
+                            const uint32_t mb = member_bit(pv[u], exact_bits, mshift);
+                            in[u] = (bitmap[mb >> 5] >> (mb & 31)) & 1u;
+                        }
+                    }
+    #pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        if (!in[u]) continue;
+                        const int32_t pos = pv[u];
+                        uint32_t h = hash_slot(pos, hshift);
+                        for (int probe = 0; probe < H; ++probe) {
+                            const uint32_t key = keys[h];
+                            if (key == 0u) break;
+                            if (key == (uint32_t)pos + 1u) {
+                                hit_s[kidx[h]] = b0 + u * kThreads;
+                                flags_s[b0 + u * kThreads] = 1;
+                                break;
+                            }
+                            h = (h + 1) & (uint32_t)(H - 1);
+                        }
+                    }
                 }
                 __syncthreads();
+
+                // ------------- P3: misses and victims (ballot scans) --------
+                // warp w owns a contiguous block of 32*seg elements of each
+                // array; element order = warp, then round, then lane.  Loads of
+                // up to 8 rounds are issued before their ballots.
+                const int segK = (k + kThreads - 1) / kThreads;
+                const int segB = (B + kThreads - 1) / kThreads;
+                const int baseK = warp * 32 * segK, baseB = warp * 32 * segB;
+                const uint32_t lt = lanemask_lt();
+                uint32_t cm = 0, cn = 0;
+                for (int s0 = 0; s0 < segK; s0 += 8) {
+                    bool pr[8];
+    #pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int i = baseK + (s0 + u) * 32 + lane;
+                        pr[u] = s0 + u < segK && i < k && hit_s[i] < 0;
+                    }
+    #pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        if (s0 + u < segK) cm += __popc(__ballot_sync(0xFFFFFFFFu, pr[u]));
+                }
+                for (int s0 = 0; s0 < segB; s0 += 8) {
+                    int ob[8];
+                    bool pr[8];
+    #pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int q = baseB + (s0 + u) * 32 + lane;
+                        ob[u] = (s0 + u < segB && q < B) ? (int)order_s[q] : -1;
+                    }
+    #pragma unroll
+                    for (int u = 0; u < 8; ++u) pr[u] = ob[u] >= 0 && !(flags_s[ob[u]] & 1);
+    #pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        if (s0 + u < segB) cn += __popc(__ballot_sync(0xFFFFFFFFu, pr[u]));
+                }
+                uint32_t total;
+                const uint32_t base = warp_counts_exscan(cm | (cn << 16), sums, &total);
+                const int m = (int)(total & 0xFFFFu);
+                const int nh = (int)(total >> 16);
+                uint32_t mr = base & 0xFFFFu, nr = base >> 16;
+                for (int s0 = 0; s0 < segK; s0 += 8) {
+                    bool pr[8];
+                    int32_t sv[8];
+    #pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int i = baseK + (s0 + u) * 32 + lane;
+                        pr[u] = s0 + u < segK && i < k && hit_s[i] < 0;
+                        sv[u] = pr[u] ? sel_s[i] : 0;
+                    }
+    #pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        if (s0 + u >= segK) break;
+                        const uint32_t bal = __ballot_sync(0xFFFFFFFFu, pr[u]);
+                        if (pr[u]) {
+                            const uint32_t rank = mr + __popc(bal & lt);
+                            mpos[rank] = sv[u];
+                            hit_s[baseK + (s0 + u) * 32 + lane] = -2 - (int32_t)rank;
+                        }
+                        mr += __popc(bal);
+                    }
+                }
+                for (int s0 = 0; s0 < segB; s0 += 8) {
+                    int ob[8];
+                    bool pr[8];
+    #pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int q = baseB + (s0 + u) * 32 + lane;
+                        ob[u] = (s0 + u < segB && q < B) ? (int)order_s[q] : -1;
+                    }
+    #pragma unroll
+                    for (int u = 0; u < 8; ++u) pr[u] = ob[u] >= 0 && !(flags_s[ob[u]] & 1);
+    #pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        if (s0 + u >= segB) break;
+                        const uint32_t bal = __ballot_sync(0xFFFFFFFFu, pr[u]);
+                        if (pr[u]) {
+                            const uint32_t rank = nr + __popc(bal & lt);
+                            const int b = ob[u];
+                            if ((int)rank < m) {
+                                mslot[rank] = b;
+                                flags_s[b] |= 2;
+                                if (with_plan) vrank_s[b] = (uint16_t)rank;
+                            } else {
+                                neworder[rank - m] = (uint16_t)b;
+                            }
+                        }
+                        nr += __popc(bal);
+                    }
+                }
+                if (tid == 0) {
+                    hdr[H_M] = (uint32_t)m;
+                    hdr[H_NH] = (uint32_t)nh;
+                    hdr[H_F] = (uint32_t)m;
+                    hdr[H_FLIST] = 0u;
+                }
+                __syncthreads();
+
+                // ------------- P3b: consume a plan --------------------------
+                if (with_plan) {
+                    const PlanHeader *ph = reinterpret_cast<const PlanHeader *>(plan_in);
+                    const int32_t *eh =
+                        reinterpret_cast<const int32_t *>(plan_in + 16 + (size_t)ireq * plan_entry_bytes(k));
+                    const bool ok = ph->magic == kPlanMagic && ph->n_req == n_req && ph->k == k &&
+                                    ph->layer == layer && eh[0] >= 0 && eh[0] <= k && eh[1] == r;
+                    const int mp = ok ? eh[0] : 0;
+                    if (!ok && tid == 0) atomicOr(p.status, HS_STATUS_PLAN);
+                    const int32_t *ppos = eh + 4;
+                    const int32_t *pslot = ppos + k;
+                    const int n = m > mp ? m : mp;
+                    for (int j = tid; j < n; j += kThreads) {
+                        const int32_t pp = j < mp ? ppos[j] : -1;
+                        const int32_t ps = j < mp ? pslot[j] : -1;
+                        if (j < m && j < mp && pp == mpos[j] && ps == mslot[j]) {
+                            atomicAdd(&hdr[H_PHIT], 1u);
+                            continue;
+                        }
+                        atomicAdd(&hdr[H_PMISS], 1u);
+                        if (j < m) {
+                            const uint32_t f = atomicAdd(&hdr[H_NF], 1u);
+                            fpos[f] = mpos[j];
+                            fslot[f] = mslot[j];
+                        }
+                        if (j < mp) {
+                            if (ps >= 0 && ps < B && pp >= 0 && (int64_t)pp < p.L) {
+                                // the copy wrote slot ps: refill it with its owner
+                                const int32_t owner = (flags_s[ps] & 2) ? mpos[vrank_s[ps]] : spos_s[ps];
+                                if (owner >= 0) {
+                                    const uint32_t f = atomicAdd(&hdr[H_NF], 1u);
+                                    fpos[f] = owner;
+                                    fslot[f] = ps;
+                                }
+                            } else {
+                                atomicOr(p.status, HS_STATUS_PLAN);
+                            }
+                        }
+                    }
+                    __syncthreads();
+                    if (tid == 0) {
+                        hdr[H_F] = hdr[H_NF];
+                        hdr[H_FLIST] = 1u;
+                    }
+                    __syncthreads();
+                }
             }
-        } else {
+            if (!speculative) break;
+
+            // ---------------- the speculative decision stands only if its
+            // inputs are unchanged now that the previous grid has completed
+            grid_dependency_wait();
+            const int r_now = req_ids ? req_ids[ireq] : ireq;
+            int stale = r_now != r;
+            for (int i = tid; i < k; i += kThreads) stale |= selr[i] != sel_s[i];
+            if (tid == 0 && !stale && r_ok) {
+                // claim the pair, then look at its counter: a resolve that held
+                // it and has let it go has moved the counter before
+                if (atomicCAS(&p.busy[pair], 0u, 1u) == 0u) {
+                    took_busy = true;
+                    stale = ld_acquire_gpu(&p.tcount[pair]) != t_seen;
+                } else {
+                    atomicOr(&hdr[H_ABORT], HS_STATUS_REQ_BUSY);
+                }
+            }
+            if (!__syncthreads_or(stale)) break;
+            // decide again on what the previous grid left
+            r = r_now;
+            r_ok = r >= 0 && r < p.R;
+            pair = (int64_t)layer * p.R + (r_ok ? r : 0);
+            host_pair = p.host + ((int64_t)(r_ok ? r : 0) * p.NL + layer) * p.L * W;
+            cache_pair = p.cache + pair * B * (int64_t)W;
+        }  // attempts
+        const uint32_t abort_bits = hdr[H_ABORT];
+        if (abort_bits != 0u) {
             // rejected request: publish -1, leave metadata and slots alone
             if (!kPlanOnly) {
                 int32_t *o = out_g + (int64_t)ireq * k;
@@ -599,6 +658,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // sbits[block] remembers which entries were staged.
         const FollowerLayout fl = follower_layout(k, W);
         int32_t *stg = reinterpret_cast<int32_t *>(smem + fl.stg) + warp * kStageMax;
+        int32_t *stgpos = reinterpret_cast<int32_t *>(smem + fl.stgpos) + warp * kStageMax;
         uint32_t *sbits = reinterpret_cast<uint32_t *>(smem + fl.sbits);
         uint8_t *stage = smem + fl.stage + (size_t)warp * fl.cap * W;
         const int nf = csize > 1 ? (int)csize - 1 : 1, f = (int)crank - 1;
@@ -630,12 +690,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t *dst = stage + (size_t)staged_n * W;
                     const uint8_t *from = host_pair + (int64_t)q * W;
                     for (int c = lane; c < CW; c += 32) cp_async16(dst + 16 * c, from + 16 * c);
-                    if (lane == 0) stg[staged_n] = blk * 32 + src;
+                    if (lane == 0) {
+                        stg[staged_n] = blk * 32 + src;
+                        stgpos[staged_n] = q;
+                    }
                     staged |= 1u << src;
                     ++staged_n;
                 }
                 if (lane == 0) sbits[blk] = staged;
             }
+        }
+        // the previous grid's writes are visible from here on; a request id
+        // that changed under the early reads voids this CTA's staging
+        grid_dependency_wait();
+        const int r_now = req_ids ? req_ids[ireq] : ireq;
+        if (r_now != r) {
+            r = r_now;
+            r_ok = r >= 0 && r < p.R;
+            pair = (int64_t)layer * p.R + (r_ok ? r : 0);
+            host_pair = p.host + ((int64_t)(r_ok ? r : 0) * p.NL + layer) * p.L * W;
+            cache_pair = p.cache + pair * B * (int64_t)W;
+            staged_n = 0;
+            for (int blk = warp; blk < nblk; blk += kWarps)
+                if (lane == 0) sbits[blk] = 0u;
         }
         __syncthreads();
     }
@@ -705,8 +782,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint16_t *lo = p.lru + pair * B;
                 for (int b = tid; b < B; b += kThreads) lo[b] = neworder[b];
                 const int F = (int)hdr[H_F];
+                // the counter moves after every metadata write of the commit:
+                // a later launch deciding early reads it before the metadata
+                __syncthreads();
                 if (tid == 0) {
-                    p.tcount[pair] = t;
+                    __threadfence();
+                    st_release_gpu(&p.tcount[pair], t);
                     unsigned long long *c = p.counters + (int64_t)layer * CTR_COUNT;
                     atomicAdd(&c[CTR_RESOLVES], 1ull);
                     atomicAdd(&c[CTR_HITS], (unsigned long long)(k - m));
@@ -753,9 +834,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int32_t *lhit = cl.map_shared_rank(hit_s, 0);
             const int32_t *lmslot = cl.map_shared_rank(mslot, 0);
             const bool abort = lh[H_ABORT] != 0u;
+            const int32_t *lsel = cl.map_shared_rank(sel_s, 0);
             const FollowerLayout fl = follower_layout(k, W);
             const int32_t *stg = reinterpret_cast<const int32_t *>(smem + fl.stg) + warp * kStageMax;
-            const uint32_t *sbits = reinterpret_cast<const uint32_t *>(smem + fl.sbits);
+            const int32_t *stgpos =
+                reinterpret_cast<const int32_t *>(smem + fl.stgpos) + warp * kStageMax;
+            uint32_t *sbits = reinterpret_cast<uint32_t *>(smem + fl.sbits);
             const uint8_t *stage = smem + fl.stage + (size_t)warp * fl.cap * W;
             int32_t *xp = reinterpret_cast<int32_t *>(smem + fl.xp);  // misses not staged
             int32_t *xs = reinterpret_cast<int32_t *>(smem + fl.xs);
@@ -766,18 +850,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             // F1: the victim slot of each staged record (-1: the leader found
             // a hit), and the leader's misses of this warp's blocks that were
             // not staged
+            // A staged record whose position is not the leader's selection
+            // (read before the wait, changed since) is dropped and fetched
+            // with the unstaged misses.
             int32_t my_slot = -1;
             if (!abort && lane < staged_n) {
-                const int32_t hsl = lhit[i0 + stg[lane]];
-                my_slot = hsl <= -2 ? lmslot[-2 - hsl] : -1;
+                const int e = stg[lane];
+                if (lsel[i0 + e] == stgpos[lane]) {
+                    const int32_t hsl = lhit[i0 + e];
+                    my_slot = hsl <= -2 ? lmslot[-2 - hsl] : -1;
+                } else {
+                    atomicAnd(&sbits[e >> 5], ~(1u << (e & 31)));
+                }
             }
+            __syncwarp();
             if (!abort) {
                 for (int blk = warp; blk < nblk; blk += kWarps) {
                     const int e = blk * 32 + lane;
                     const int32_t hsl = e < ns ? lhit[i0 + e] : -1;
                     if (hsl <= -2 && !((sbits[blk] >> lane) & 1u)) {
                         const uint32_t x = atomicAdd(&hdr[H_NX], 1u);
-                        xp[x] = selr[i0 + e];
+                        xp[x] = lsel[i0 + e];
                         xs[x] = lmslot[-2 - hsl];
                     }
                 }

@@ -150,17 +150,24 @@ def hs_link_probe(nbytes: int, reps: int = 10, record_bytes: int = 1152):
     return a.value, b.value
 
 
-def hs_attention_workspace_bytes(n_req: int, k: int, heads: int) -> int:
-    return int(_lib().hs_attention_workspace_bytes(n_req, k, heads))
-
-
-def hs_sparse_attention(q, cache, cache_rows, idx, n_req, k, heads, scale, workspace, out,
+def hs_sparse_attention(q, cache, cache_rows, idx, n_req, k, heads, scale, out,
                         stream=None) -> None:
     """Attention of q [n_req][heads][576] bf16 over the published rows idx
     [n_req][k] of a layer's cache; fp32 out [n_req][heads][512]."""
     _check(_lib().hs_sparse_attention(_ptr(q), _ptr(cache), cache_rows, _ptr(idx), n_req, k,
-                                      heads, scale, _ptr(workspace), _ptr(out), _stream(stream)),
+                                      heads, scale, _ptr(out), _stream(stream)),
            "hs_sparse_attention")
+
+
+HS_ATTN_STATUS_TIMEOUT = 0x1
+
+
+def hs_attention_status() -> int:
+    """HS_ATTN_STATUS_* bits set by attention calls since the last query
+    (synchronises the device, clears the bits)."""
+    v = ctypes.c_uint32()
+    _check(_lib().hs_attention_status(ctypes.byref(v)), "hs_attention_status")
+    return int(v.value)
 
 
 HS_NOALLOC_MAX_REQUESTS = 4096

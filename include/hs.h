@@ -233,17 +233,27 @@ int hs_link_probe(size_t bytes, int32_t reps, int32_t record_bytes, double *h2d_
  * resolve rejected publishes -1); a head with no valid key gets zeros.
  * d_q: device bf16 [n_req][heads][576]; d_cache: a layer's cache,
  * cache_rows rows of 1152 bytes (hs_device_views); d_idx: device int32
- * [n_req][k]; d_workspace: hs_attention_workspace_bytes(n_req, k, heads)
- * bytes of device memory the caller owns (partial results of the key
- * chunks, overwritten by every call); d_out: device fp32.  All pointers
- * 16-byte aligned.  heads must be a positive multiple of 16.  Two kernels
- * are enqueued on `stream`; nothing is allocated.  Errors:
- * HS_ERR_INVALID_ARG, HS_ERR_CUDA.
+ * [n_req][k]; d_out: device fp32.  d_q, d_cache and d_out 16-byte
+ * aligned; n_req <= 65535; heads a positive multiple of 16.  One kernel is
+ * enqueued on `stream` (a thread-block cluster per request and 16 heads,
+ * whose CTAs split the keys and merge their partial results on chip);
+ * nothing is allocated and no scratch memory is needed.  The split of the
+ * keys depends on (n_req, k, heads) and the device only, so equal inputs
+ * give bit-identical outputs.  A pipeline wait that runs out of time (one
+ * second) makes the affected outputs NaN and sets HS_ATTN_STATUS_TIMEOUT
+ * (see hs_attention_status).  Errors: HS_ERR_INVALID_ARG, HS_ERR_CUDA.
  */
-size_t hs_attention_workspace_bytes(int32_t n_req, int32_t k, int32_t heads);
 int hs_sparse_attention(const void *d_q, const void *d_cache, int64_t cache_rows,
                         const int32_t *d_idx, int32_t n_req, int32_t k, int32_t heads,
-                        float scale, void *d_workspace, float *d_out, void *stream);
+                        float scale, float *d_out, void *stream);
+
+#define HS_ATTN_STATUS_TIMEOUT 0x1u
+
+/* Synchronises the device, then returns in *status and clears the
+ * HS_ATTN_STATUS_* bits that hs_sparse_attention calls have set on the
+ * current device since the last call (0: none).  Errors:
+ * HS_ERR_INVALID_ARG (status == NULL), HS_ERR_CUDA. */
+int hs_attention_status(uint32_t *status);
 
 /* Kernels launched per call of hs_resolve / hs_prefetch_plan /
  * hs_prefetch_copy (for launch accounting; always 1 in this build). */

@@ -79,15 +79,15 @@ def test_create_pool_refuses_over_host_limit(lib):
 
 def test_attention_argument_checks(lib):
     f = lib.hs_sparse_attention
-    assert f(16, 16, 10, 16, 1, 10, 8, 1.0, 16, 16, None) == hs.HS_ERR_INVALID_ARG   # heads
-    assert f(16, 16, 10, 16, 1, 0, 16, 1.0, 16, 16, None) == hs.HS_ERR_INVALID_ARG   # k = 0
-    assert f(16, 16, 0, 16, 1, 10, 16, 1.0, 16, 16, None) == hs.HS_ERR_INVALID_ARG   # no rows
-    assert f(8, 16, 10, 16, 1, 10, 16, 1.0, 16, 16, None) == hs.HS_ERR_INVALID_ARG   # alignment
-    assert f(None, 16, 10, 16, 1, 10, 16, 1.0, 16, 16, None) == hs.HS_ERR_INVALID_ARG
-    assert f(16, 16, 10, 16, 0, 10, 16, 1.0, 16, 16, None) == hs.HS_OK   # n_req = 0: no-op
-    # partial results: 512 values + max + sum (+ pad) per head and 128-key chunk
-    assert lib.hs_attention_workspace_bytes(8, 2048, 16) == 8 * 16 * 16 * 516 * 4
-    assert lib.hs_attention_workspace_bytes(2, 300, 32) == 2 * 3 * 32 * 516 * 4
+    assert f(16, 16, 10, 16, 1, 10, 8, 1.0, 16, None) == hs.HS_ERR_INVALID_ARG   # heads
+    assert f(16, 16, 10, 16, 1, 0, 16, 1.0, 16, None) == hs.HS_ERR_INVALID_ARG   # k = 0
+    assert f(16, 16, 0, 16, 1, 10, 16, 1.0, 16, None) == hs.HS_ERR_INVALID_ARG   # no rows
+    assert f(8, 16, 10, 16, 1, 10, 16, 1.0, 16, None) == hs.HS_ERR_INVALID_ARG   # alignment
+    assert f(16, 16, 10, 16, 1, 10, 16, 1.0, 8, None) == hs.HS_ERR_INVALID_ARG
+    assert f(None, 16, 10, 16, 1, 10, 16, 1.0, 16, None) == hs.HS_ERR_INVALID_ARG
+    assert f(16, 16, 10, 16, 70000, 10, 16, 1.0, 16, None) == hs.HS_ERR_INVALID_ARG
+    assert f(16, 16, 10, 16, 0, 10, 16, 1.0, 16, None) == hs.HS_OK   # n_req = 0: no-op
+    assert lib.hs_attention_status(None) == hs.HS_ERR_INVALID_ARG
 
 
 def test_calls_on_null_pool_are_rejected(lib):

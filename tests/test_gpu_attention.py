@@ -9,7 +9,10 @@
 * attention over the published slots is bit-identical to attention over the
   same records copied straight from the host pool in selection order -- the
   exactness claim, on the GPU;
-* rows outside the cache (a rejected request publishes -1) are masked.
+* rows outside the cache (a rejected request publishes -1) are masked;
+* ragged key counts (one key, a partial pipeline stage, a split boundary),
+  several head groups and batch sizes that change the split of the keys;
+  repeated calls are bit-identical and raise no status bit.
 """
 import numpy as np
 import pytest
@@ -47,11 +50,10 @@ def _setup(R=4, k=300, heads=32, steps=2, seed=3):
 
 def _attend(cache, rows, idx, q16, R, k, heads):
     q = torch.from_numpy(q16.view(np.int16)).cuda()
-    ws = torch.empty(hs.hs_attention_workspace_bytes(R, k, heads), dtype=torch.uint8,
-                     device="cuda")
-    out = torch.empty((R, heads, 512), dtype=torch.float32, device="cuda")
-    hs.hs_sparse_attention(q, cache, rows, idx, R, k, heads, SCALE, ws, out)
+    out = torch.full((R, heads, 512), float("nan"), dtype=torch.float32, device="cuda")
+    hs.hs_sparse_attention(q, cache, rows, idx, R, k, heads, SCALE, out)
     torch.cuda.synchronize()
+    assert hs.hs_attention_status() == 0
     return out.cpu().numpy()
 
 
@@ -101,3 +103,28 @@ def test_masked_rows():
         for h in range(heads):
             ref = sparse_attention(rec, 1, q[1, h])[0]
             assert np.max(np.abs(got[1, h] - ref)) <= 4 * 2.0 ** -9 * vmax
+
+
+@pytest.mark.parametrize("R,k,heads", [(1, 1, 16), (3, 33, 48), (2, 65, 16), (5, 1000, 16),
+                                       (40, 96, 16), (1, 2048, 128)])
+def test_ragged_shapes_against_oracle(R, k, heads):
+    w = configs.DSA_MLA.with_(n_requests=1, n_layers=1, n_positions=5000)
+    rng = np.random.default_rng(R * 1000 + k + heads)
+    rows = 4096
+    table = records.gen(w, 0, 0, np.arange(rows))          # a dense cache of records
+    idx = np.stack([rng.choice(rows, k, replace=False) for _ in range(R)]).astype(np.int32)
+    if k > 4:
+        idx[0, 1::5] = -1                                    # masked keys
+    q16 = _bf16_round(rng.standard_normal((R, heads, 576)).astype(np.float32))
+    cache = torch.from_numpy(table).cuda()
+    didx = torch.from_numpy(idx).cuda()
+    got = _attend(cache, rows, didx, q16, R, k, heads)
+    again = _attend(cache, rows, didx, q16, R, k, heads)
+    assert np.array_equal(got.view(np.uint32), again.view(np.uint32))
+    q = _bf16_to_f64(q16)
+    for r in range(R):
+        rec = table[idx[r][idx[r] >= 0]]
+        vmax = np.abs(records.decode(w, rec)[:, :512]).max()
+        for h in range(heads):
+            ref = sparse_attention(rec, 1, q[r, h])[0]
+            assert np.max(np.abs(got[r, h] - ref)) <= 4 * 2.0 ** -9 * vmax, (r, h)

@@ -367,3 +367,73 @@ def test_host_records_layout():
         assert gap == w.n_positions * w.record_bytes   # host[r][l][pos][W]
         a[:] = records.gen(w, 1, 1, np.arange(w.n_positions))
         assert np.array_equal(pool.host_records(1, 1)[17], records.gen(w, 1, 1, [17])[0])
+
+
+@pytest.mark.parametrize("cluster", ["1", "4", ""])
+@pytest.mark.parametrize("tight", [False, True])
+def test_back_to_back_resolves_of_one_layer(cluster, tight, monkeypatch):
+    """Many resolves of the same pairs enqueued back to back with no host
+    synchronisation.  Each launch starts while the previous one still runs
+    and decides on metadata that launch is about to change; the decision
+    must be found stale and taken again, so every step's published slots,
+    the final metadata and the slot contents equal the oracle's.  With
+    B = k every slot that is not selected is evicted at every step."""
+    monkeypatch.setenv("HS_CLUSTER", cluster)
+    from workloads import traces
+    w = configs.DSA_MLA.with_(n_requests=3, n_layers=1, n_positions=12000, k=256,
+                              slots=256 if tight else 512, steps=30, local_window=600)
+    sel = traces.generate(w)
+    orc = _oracles(w)
+    with hs.Pool.for_workload(w) as pool:
+        fill_selected(pool, w, sel)
+        dsel = torch.from_numpy(np.ascontiguousarray(sel[:, :, 0])).cuda()   # [T][R][k]
+        out = torch.empty((w.steps, w.n_requests, w.k), dtype=torch.int32, device="cuda")
+        torch.cuda.synchronize()
+        for t in range(w.steps):
+            pool.resolve(0, dsel[t], out[t])
+        got = out.cpu().numpy()
+        misses = 0
+        for t in range(w.steps):
+            for r in range(w.n_requests):
+                rc, o, m = orc[(r, 0)].resolve(sel[t, r, 0], out_base=r * w.slots)
+                assert rc == OK and np.array_equal(got[t, r], o), (t, r)
+                misses += m
+        st = pool.stats(0)
+        assert st["resolves"] == w.steps * w.n_requests and st["misses"] == misses
+        for r in range(w.n_requests):
+            check_metadata(pool, w, 0, r, orc[(r, 0)], w.steps)
+            check_cache(pool, w, 0, r, orc[(r, 0)].slot_pos)
+
+
+def test_interleaved_layers_without_synchronisation():
+    """Launch orders that alternate layers and repeat them (0 0 1 0 1 1 ...)
+    with no host synchronisation: overlapping launches of other layers keep
+    their early decisions, those of the same layer take them again."""
+    from workloads import traces
+    w = configs.DSA_MLA.with_(n_requests=2, n_layers=2, n_positions=10000, k=192, slots=384,
+                              steps=24, local_window=500)
+    sel = traces.generate(w)
+    orc = _oracles(w)
+    order = [0, 0, 1, 0, 1, 1]
+    with hs.Pool.for_workload(w) as pool:
+        fill_selected(pool, w, sel)
+        dsel = torch.from_numpy(np.ascontiguousarray(sel.transpose(0, 2, 1, 3))).cuda()
+        launches = []   # (t, layer) in launch order; step t of a layer uses sel[t]
+        nxt = [0, 0]
+        while min(nxt) < w.steps:
+            for l in order:
+                if nxt[l] < w.steps:
+                    launches.append((nxt[l], l))
+                    nxt[l] += 1
+        out = torch.empty((len(launches), w.n_requests, w.k), dtype=torch.int32, device="cuda")
+        torch.cuda.synchronize()
+        for i, (t, l) in enumerate(launches):
+            pool.resolve(l, dsel[t, l], out[i])
+        got = out.cpu().numpy()
+        for i, (t, l) in enumerate(launches):
+            for r in range(w.n_requests):
+                rc, o, _ = orc[(r, l)].resolve(sel[t, r, l], out_base=r * w.slots)
+                assert rc == OK and np.array_equal(got[i, r], o), (i, t, r, l)
+        for (r, l), p in orc.items():
+            check_metadata(pool, w, l, r, p, w.steps)
+            check_cache(pool, w, l, r, p.slot_pos)

@@ -922,8 +922,9 @@ cudaError_t launch_resolve(const DevPool &p, int layer, int n_req, const int32_t
     attr[0].val.clusterDim.x = (unsigned)cluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    // the launch may overlap the tail of the previous grid in the stream;
-    // the kernel waits for that grid before touching global memory
+    // the launch may overlap the previous grid in the stream: the kernel
+    // reads its inputs early and writes no global memory before that grid
+    // has completed
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;

@@ -15,8 +15,10 @@
 // In every CTA a producer warp gathers its rows 32 at a time into a
 // two-stage shared-memory ring with one bulk copy per row (the TMA engine,
 // completion counted in bytes on an mbarrier; the rows are scattered over the
-// cache, so there is no tile to describe), reading the slot indices two
-// stages ahead; four consumer warps compute, per stage, S = Q K^T with
+// cache, so there is no tile to describe; 16-byte cp.async copies from the
+// producer's lanes were measured slower, alone and shared with the bulk
+// copies), reading the slot indices two stages ahead; four consumer warps
+// compute, per stage, S = Q K^T with
 // warp-level bf16 MMAs (fp32 accumulation; each warp holds a quarter of the
 // 576 query columns in registers and the four partial S tiles are summed
 // through shared memory), an online softmax, and O += P V with P kept in
@@ -117,7 +119,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase of `bar` with the given parity; false after the limit.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Inlined: a call would make the caller settle its loads in flight first.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     while (!mbar_try_wait(bar, parity))
@@ -226,17 +229,21 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
 
     if (warp == kConsumerWarps) {
         // ---------------- producer: one bulk copy per row ----------------
+        // the raw slot index of this lane's row in stage st (-1 past the
+        // split); it is checked only when used, so the load stays in flight
         auto load_row = [&](int st) {
             const int key = key0 + st * kStageKeys + lane;
             int32_t row = -1;
-            if (st < nstage && key < key1) {
-                row = idx[(int64_t)r * k + key];
-                if (row < 0 || (int64_t)row >= cache_rows) row = -1;  // masked key
-            }
+            if (st < nstage && key < key1) row = __ldg(idx + (int64_t)r * k + key);
             return row;
         };
-        static_assert(kStages == 2, "the index prefetch below keeps two stages ahead");
-        int32_t row_a = load_row(0), row_b = load_row(1);
+        // Slot indices are read kStages stages ahead, each into the register
+        // its stage will use: the loop is unrolled by kStages so that no
+        // register holding a load in flight is ever copied (a copy would wait
+        // for the load).
+        int32_t rows[kStages];
+#pragma unroll
+        for (int j = 0; j < kStages; ++j) rows[j] = load_row(j);
         if (lane == 0) mbar_arrive_expect_tx(q_bar, kGroup * kRowBytes);
         __syncwarp();
         if (lane < kGroup)
@@ -244,29 +251,35 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
                      q + ((int64_t)r * heads + (int64_t)g * kGroup + lane) * kRowBytes, kRowBytes,
                      q_bar);
         int issued = 0;
-        for (int st = 0; st < nstage; ++st) {
-            const int b = st % kStages;
-            const int32_t row = row_a;
-            row_a = row_b;
-            row_b = load_row(st + 2);  // in flight while this stage waits and issues
-            if (st >= kStages) {
-                // the consumers released this buffer's previous stage
-                const bool free_ok = mbar_wait(empty_bar(b), ((st / kStages) - 1) & 1);
-                if (!__all_sync(0xFFFFFFFFu, free_ok)) {
-                    ok = false;
-                    break;
+        for (int st0 = 0; st0 < nstage && ok; st0 += kStages) {
+#pragma unroll
+            for (int b = 0; b < kStages; ++b) {
+                const int st = st0 + b;
+                if (st >= nstage) break;
+                if (st >= kStages) {
+                    // the consumers released this buffer's previous stage
+                    const bool free_ok = mbar_wait(empty_bar(b), ((st / kStages) - 1) & 1);
+                    if (!__all_sync(0xFFFFFFFFu, free_ok)) {
+                        ok = false;
+                        break;
+                    }
                 }
+                const int32_t raw = rows[b];
+                rows[b] = load_row(st + kStages);  // in flight for kStages stages
+                const bool use = raw >= 0 && (int64_t)raw < cache_rows;  // else a masked key
+                const uint32_t valid = __ballot_sync(0xFFFFFFFFu, use);
+                if (lane == 0) {
+                    maskw[b] = valid;
+                    mbar_arrive_expect_tx(full_bar(b), kStageKeys * kRowBytes);
+                }
+                __syncwarp();
+                const void *src = use
+                                      ? static_cast<const void *>(cache + (int64_t)raw * kRowBytes)
+                                      : static_cast<const void *>(g_zero_row);
+                bulk_row(smem_addr(kv_s + (b * kStageKeys + lane) * kPitch), src, kRowBytes,
+                         full_bar(b));
+                issued = st + 1;
             }
-            const uint32_t valid = __ballot_sync(0xFFFFFFFFu, row >= 0);
-            if (lane == 0) {
-                maskw[b] = valid;
-                mbar_arrive_expect_tx(full_bar(b), kStageKeys * kRowBytes);
-            }
-            __syncwarp();
-            const void *src = row >= 0 ? static_cast<const void *>(cache + (int64_t)row * kRowBytes)
-                                       : static_cast<const void *>(g_zero_row);
-            bulk_row(smem_addr(kv_s + (b * kStageKeys + lane) * kPitch), src, kRowBytes, full_bar(b));
-            issued = st + 1;
         }
         // copies still in flight must land before the ring is reused or the
         // CTA exits: in a normal run the consumers have already waited for

@@ -130,12 +130,12 @@ __host__ __device__ inline SmemLayout smem_layout(int B, int k, bool with_plan, 
 }
 
 // A follower CTA of a resolve cluster needs none of the leader's arrays.
-// After the 256-byte header it keeps: the share entries each warp staged
-// and their positions (kStageMax per warp each), one staged-bit word per
-// block of 32 share entries,
+// After the 256-byte header it keeps: for each record it staged, the share
+// entry and the position (up to kStageCap records, a pool shared by its
+// warps), one staged-bit word per block of 32 share entries,
 // the list (positions, slots) of misses it did not stage, and then the
-// staging area for whole records, `cap` records per warp.
-constexpr int kStageMax = 32;
+// staging area for whole records, `cap` records in all.
+constexpr int kStageCap = 256;
 struct FollowerLayout {
     uint32_t stg, stgpos, sbits, xp, xs, stage;
     int cap;
@@ -144,8 +144,8 @@ struct FollowerLayout {
 __host__ __device__ inline FollowerLayout follower_lists(int k) {
     FollowerLayout f;
     uint32_t o = 256;
-    f.stg = o;   o += 4u * kWarps * kStageMax;
-    f.stgpos = o; o += 4u * kWarps * kStageMax;
+    f.stg = o;   o += 4u * kStageCap;
+    f.stgpos = o; o += 4u * kStageCap;
     f.sbits = o; o += align16(4u * (uint32_t)((k + 31) / 32));
     f.xp = o;    o += align16(4u * (uint32_t)k);
     f.xs = o;    o += align16(4u * (uint32_t)k);
@@ -175,6 +175,7 @@ enum Hdr : int {
     H_PHIT = 8,      // plan-mode plan hits
     H_G = 9,         // follower: predicted misses in its share
     H_NX = 10,       // follower: leader misses it did not predict
+    H_NSTG = 11,     // follower: staging slots handed out (may exceed the capacity)
     H_SUMS = 16,     // kWarps scan sums from here
 };
 

@@ -184,8 +184,8 @@ __device__ __forceinline__ uint32_t dynamic_smem_bytes() {
 __device__ __forceinline__ FollowerLayout follower_layout(int k, int W) {
     FollowerLayout f = follower_lists(k);
     const uint32_t total = dynamic_smem_bytes();
-    const int cap = total > f.stage ? (int)((total - f.stage) / ((uint32_t)kWarps * (uint32_t)W)) : 0;
-    f.cap = cap < kStageMax ? cap : kStageMax;
+    const int cap = total > f.stage ? (int)((total - f.stage) / (uint32_t)W) : 0;
+    f.cap = cap < kStageCap ? cap : kStageCap;
     return f;
 }
 
@@ -316,9 +316,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     int64_t pair = (int64_t)layer * p.R + (r_ok ? r : 0);
     const uint8_t *host_pair = p.host + ((int64_t)(r_ok ? r : 0) * p.NL + layer) * p.L * W;
     uint8_t *cache_pair = p.cache + pair * B * (int64_t)W;
-
-    // follower state: records this warp staged (warp-uniform)
-    int staged_n = 0;
 
     if (crank == 0) {
         bool took_busy = false;  // (thread 0)
@@ -653,14 +650,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Warp w takes blocks of 32 consecutive share entries (w, w + 16,
         // ...).  A lane reads its selection and the page-table entry of the
         // position; -1 predicts a miss.  For every predicted miss the warp
-        // issues cp.async copies of the record from the mapped host pool
-        // into its own staging area of shared memory, up to `cap` records;
-        // sbits[block] remembers which entries were staged.
+        // takes a slot of the CTA's staging pool (one atomic per block) and
+        // issues cp.async copies of the record from the mapped host pool into
+        // it, while the pool lasts; sbits[block] remembers which entries
+        // were staged.
         const FollowerLayout fl = follower_layout(k, W);
-        int32_t *stg = reinterpret_cast<int32_t *>(smem + fl.stg) + warp * kStageMax;
-        int32_t *stgpos = reinterpret_cast<int32_t *>(smem + fl.stgpos) + warp * kStageMax;
+        int32_t *stg = reinterpret_cast<int32_t *>(smem + fl.stg);
+        int32_t *stgpos = reinterpret_cast<int32_t *>(smem + fl.stgpos);
         uint32_t *sbits = reinterpret_cast<uint32_t *>(smem + fl.sbits);
-        uint8_t *stage = smem + fl.stage + (size_t)warp * fl.cap * W;
+        uint8_t *stage = smem + fl.stage;
         const int nf = csize > 1 ? (int)csize - 1 : 1, f = (int)crank - 1;
         const int i0 = (int)((int64_t)f * k / nf), i1 = (int)((int64_t)(f + 1) * k / nf);
         const int ns = i1 - i0;
@@ -682,20 +680,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int blk = blk0 + u * kWarps;
                 if (blk >= nblk) break;
                 uint32_t mask = __ballot_sync(0xFFFFFFFFu, ptv[u] == -1);
+                uint32_t base = 0;
+                if (lane == 0 && mask) base = atomicAdd(&hdr[H_NSTG], (uint32_t)__popc(mask));
+                int slot = (int)__shfl_sync(0xFFFFFFFFu, base, 0);
                 uint32_t staged = 0;
-                while (mask && staged_n < fl.cap) {
+                while (mask && slot < fl.cap) {
                     const int src = __ffs(mask) - 1;
                     mask &= mask - 1;
                     const int32_t q = __shfl_sync(0xFFFFFFFFu, pos[u], src);
-                    uint8_t *dst = stage + (size_t)staged_n * W;
+                    uint8_t *dst = stage + (size_t)slot * W;
                     const uint8_t *from = host_pair + (int64_t)q * W;
                     for (int c = lane; c < CW; c += 32) cp_async16(dst + 16 * c, from + 16 * c);
                     if (lane == 0) {
-                        stg[staged_n] = blk * 32 + src;
-                        stgpos[staged_n] = q;
+                        stg[slot] = blk * 32 + src;
+                        stgpos[slot] = q;
                     }
                     staged |= 1u << src;
-                    ++staged_n;
+                    ++slot;
                 }
                 if (lane == 0) sbits[blk] = staged;
             }
@@ -710,9 +711,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             pair = (int64_t)layer * p.R + (r_ok ? r : 0);
             host_pair = p.host + ((int64_t)(r_ok ? r : 0) * p.NL + layer) * p.L * W;
             cache_pair = p.cache + pair * B * (int64_t)W;
-            staged_n = 0;
-            for (int blk = warp; blk < nblk; blk += kWarps)
-                if (lane == 0) sbits[blk] = 0u;
+            __syncthreads();  // every warp is done staging
+            if (tid == 0) hdr[H_NSTG] = 0u;
+            for (int blk = tid; blk < nblk; blk += kThreads) sbits[blk] = 0u;
         }
         __syncthreads();
     }
@@ -836,11 +837,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool abort = lh[H_ABORT] != 0u;
             const int32_t *lsel = cl.map_shared_rank(sel_s, 0);
             const FollowerLayout fl = follower_layout(k, W);
-            const int32_t *stg = reinterpret_cast<const int32_t *>(smem + fl.stg) + warp * kStageMax;
-            const int32_t *stgpos =
-                reinterpret_cast<const int32_t *>(smem + fl.stgpos) + warp * kStageMax;
+            int32_t *stg = reinterpret_cast<int32_t *>(smem + fl.stg);
+            const int32_t *stgpos = reinterpret_cast<const int32_t *>(smem + fl.stgpos);
             uint32_t *sbits = reinterpret_cast<uint32_t *>(smem + fl.sbits);
-            const uint8_t *stage = smem + fl.stage + (size_t)warp * fl.cap * W;
+            const uint8_t *stage = smem + fl.stage;
+            const int nstaged = min((int)hdr[H_NSTG], fl.cap);
             int32_t *xp = reinterpret_cast<int32_t *>(smem + fl.xp);  // misses not staged
             int32_t *xs = reinterpret_cast<int32_t *>(smem + fl.xs);
             const int nf = csize > 1 ? (int)csize - 1 : 1, f = (int)crank - 1;
@@ -848,22 +849,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int ns = i1 - i0;
             const int nblk = (ns + 31) >> 5;
             // F1: the victim slot of each staged record (-1: the leader found
-            // a hit), and the leader's misses of this warp's blocks that were
-            // not staged
+            // a hit) replaces its share entry in stg, and the leader's misses
+            // of this warp's blocks that were not staged go to the x list.
             // A staged record whose position is not the leader's selection
             // (read before the wait, changed since) is dropped and fetched
             // with the unstaged misses.
-            int32_t my_slot = -1;
-            if (!abort && lane < staged_n) {
-                const int e = stg[lane];
-                if (lsel[i0 + e] == stgpos[lane]) {
-                    const int32_t hsl = lhit[i0 + e];
-                    my_slot = hsl <= -2 ? lmslot[-2 - hsl] : -1;
-                } else {
-                    atomicAnd(&sbits[e >> 5], ~(1u << (e & 31)));
+            if (!abort) {
+                for (int s = tid; s < nstaged; s += kThreads) {
+                    const int e = stg[s];
+                    int32_t slot = -1;
+                    if (lsel[i0 + e] == stgpos[s]) {
+                        const int32_t hsl = lhit[i0 + e];
+                        slot = hsl <= -2 ? lmslot[-2 - hsl] : -1;
+                    } else {
+                        atomicAnd(&sbits[e >> 5], ~(1u << (e & 31)));
+                    }
+                    stg[s] = slot;
                 }
             }
-            __syncwarp();
+            __syncthreads();
             if (!abort) {
                 for (int blk = warp; blk < nblk; blk += kWarps) {
                     const int e = blk * 32 + lane;
@@ -878,21 +882,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncthreads();
             cluster_arrive_relaxed();  // phase B: done reading the leader
             cp_async_wait_all();       // no copy into shared memory outlives the CTA
+            __syncthreads();           // every thread's staged copies have landed
             if (!abort) {
-                // F2: staged records have landed; one bulk copy per record
-                // from shared memory to its victim slot
+                // F2: one bulk copy per staged record from shared memory to
+                // its victim slot, issued by the thread that owns the record
                 fence_proxy_async_shared();
-                __syncwarp();
-                for (int s = 0; s < staged_n; ++s) {
-                    const int32_t slot = __shfl_sync(0xFFFFFFFFu, my_slot, s);
-                    if (lane == 0 && slot >= 0)
+                bool stored = false;
+                for (int s = tid; s < nstaged; s += kThreads) {
+                    const int32_t slot = stg[s];
+                    if (slot >= 0) {
                         bulk_store(cache_pair + (int64_t)slot * W, stage + (size_t)s * W, W);
+                        stored = true;
+                    }
                 }
-                if (lane == 0) bulk_commit();
+                if (stored) bulk_commit();
                 // F3: misses that were not staged
                 const int nx = (int)hdr[H_NX];
                 if (nx > 0) fetch_records(host_pair, cache_pair, xp, xs, nx, W, tid, kThreads);
-                if (lane == 0) bulk_wait_read();  // shared memory is read before the CTA ends
+                if (stored) bulk_wait_read();  // shared memory is read before the CTA ends
             }
         }
         cluster_wait();  // phase B: no CTA leaves while the leader is being read
@@ -900,6 +907,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 }  // namespace
+
+// Largest dynamic shared memory of a block on the current device (cached).
+uint32_t device_smem_optin() {
+    static int cached_dev = -1;
+    static uint32_t cached = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev != cached_dev) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return 0;
+        cached = (uint32_t)v;
+        cached_dev = dev;
+    }
+    return cached;
+}
 
 cudaError_t prepare_kernels(size_t max_smem) {
     cudaError_t e = cudaFuncSetAttribute(resolve_kernel<false>,
@@ -915,7 +938,15 @@ cudaError_t launch_resolve(const DevPool &p, int layer, int n_req, const int32_t
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(n_req * cluster), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = resolve_smem_bytes(p.B, k, plan != nullptr, p.L);
+    // A plain launch takes all the shared memory a CTA may have: the CTA is
+    // alone on its SM anyway (512 threads x 72 registers), and the followers
+    // stage more records before the leader decides.
+    uint32_t smem = resolve_smem_bytes(p.B, k, plan != nullptr, p.L);
+    if (!plan) {
+        const uint32_t most = device_smem_optin();
+        if (most > smem) smem = most;
+    }
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;

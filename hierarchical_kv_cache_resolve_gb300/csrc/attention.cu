@@ -30,6 +30,7 @@
 // the grid covers the GPU once.
 #include <algorithm>
 #include <cstdint>
+#include <mutex>
 
 #include <cooperative_groups.h>
 
@@ -527,7 +528,9 @@ int nsplit_for(int n_req, int k, int heads, const DeviceInfo &di) {
 // clusters of each size the device keeps co-resident (16-CTA clusters where
 // non-portable sizes are allowed).
 cudaError_t device_info(DeviceInfo *out) {
+    static std::mutex mu;
     static DeviceInfo cached;
+    std::lock_guard<std::mutex> lock(mu);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;

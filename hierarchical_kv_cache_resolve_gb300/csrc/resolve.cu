@@ -39,6 +39,8 @@
 // relative order and appends the victims (stamp 2t-1) and then the hits
 // (stamp 2t), each group in slot order -- exactly the (stamp, slot) order of
 // the new stamps -- so the victims are always the first m non-hit entries.
+#include <mutex>
+
 #include <cooperative_groups.h>
 
 #include "hs.h"
@@ -910,8 +912,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Largest dynamic shared memory of a block on the current device (cached).
 uint32_t device_smem_optin() {
+    static std::mutex mu;
     static int cached_dev = -1;
     static uint32_t cached = 0;
+    std::lock_guard<std::mutex> lock(mu);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     if (dev != cached_dev) {

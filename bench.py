@@ -240,6 +240,28 @@ def time_oracle(w, n_pairs: int, steps: int, threads: int):
     return n / wall, wall, n, fetched
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the
+    machine type)."""
+    import platform
+    import subprocess
+    try:
+        outp = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in outp.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine()
+
+
 def cpu_baseline(w, threads: int, epochs: int = 4):
     """The oracle over the whole trace of every pair, replayed `epochs` times
     back to back (steps past the end wrap around, as in the GPU passes):
@@ -247,7 +269,12 @@ def cpu_baseline(w, threads: int, epochs: int = 4):
     pairs = w.n_requests * w.n_layers
     steps = epochs * w.steps
     value, wall, n, fetched = time_oracle(w, pairs, steps, threads)
+    one, one_wall, one_n, _ = time_oracle(w, 1, steps, 1)
     return {"value": value, "unit": "resolves/s", "cores": threads, "kind": "oracle",
+            "cpu_model": cpu_model(),
+            "single_thread": {"value": one, "unit": "resolves/s",
+                              "sample": f"one (request, layer) pair x {steps} steps, one thread",
+                              "wall_s": one_wall},
             "sample": (f"all {pairs} (request, layer) pairs x {steps} steps ({epochs} passes "
                        f"over the {w.name} trace; {n} resolves, {fetched / 1e9:.2f} GB of "
                        f"misses copied), one thread per pair, {threads} threads"),
@@ -302,7 +329,17 @@ def run_gpu(args, w, rank, world, dist_on):
             for l in range(NL):
                 hs.hs_resolve(pool.handle, l, R, None, dsel[t, l], k, out[l], None, cap)
         graphs.append(g)
-    for s in range(Wm):
+    # step 0 from an empty cache (every selection misses), timed on its own;
+    # it is the first of the warm-up steps
+    flush(0)
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record(main)
+    graphs[0].replay()
+    c1.record(main)
+    torch.cuda.synchronize()
+    cold_ms = c0.elapsed_time(c1)
+    st_cold = pool.stats()
+    for s in range(1, Wm):
         flush(s)
         graphs[s % T].replay()
     st0 = pool.stats()
@@ -471,6 +508,13 @@ def run_gpu(args, w, rank, world, dist_on):
             "what": "per step one graph replay (pinned H2D of the step's selections, "
                     "hs_resolve per layer, D2H of the published slots) and a stream "
                     "synchronize; wall clock",
+        },
+        "cold_step": {
+            "what": "step 0 from an empty cache (every selection misses), one graph replay, "
+                    "L2 flushed; not in `value`",
+            "ms": cold_ms, "resolves_per_s": R * NL / (cold_ms / 1e3),
+            "misses": st_cold["misses"],
+            "miss_fetch_gbs": st_cold["fetched_bytes"] / (cold_ms / 1e3) / 1e9,
         },
         "gpu_launches": K * launches_per_step,
         "clocks": sampler.summary(),

@@ -12,22 +12,26 @@
 // Flash-decoding split over a gather pipeline, merged inside a thread-block
 // cluster: the C CTAs of a cluster share one request and 16 of its query
 // heads, each owning a contiguous range of the request's k published rows.
-// In every CTA a producer warp gathers its rows 32 at a time into a
-// two-stage shared-memory ring with one bulk copy per row (the TMA engine,
-// completion counted in bytes on an mbarrier; the rows are scattered over the
-// cache, so there is no tile to describe; 16-byte cp.async copies from the
-// producer's lanes were measured slower, alone and shared with the bulk
-// copies), reading the slot indices two stages ahead; four consumer warps
-// compute, per stage, S = Q K^T with
-// warp-level bf16 MMAs (fp32 accumulation; each warp holds a quarter of the
-// 576 query columns in registers and the four partial S tiles are summed
-// through shared memory), an online softmax, and O += P V with P kept in
-// registers.  The C partial results (unnormalised O, row maximum and sum)
-// are merged through distributed shared memory, each CTA producing 512/C of
-// the value columns, in a fixed order.  The work is bound by the gathered
-// bytes (about 30 flops per byte at 16 heads), so the kernel is built around
-// keeping the gather busy: two CTAs per SM, and a split count chosen so that
-// the grid covers the GPU once.
+//
+// Gather.  In every CTA a producer warp moves its rows 32 at a time into a
+// two-stage shared-memory ring, one bulk copy per row (the TMA engine;
+// completion counted in bytes on the stage's mbarrier).  The rows are
+// scattered over the cache, so there is no tile to describe.  The slot
+// indices are read two stages ahead.  (16-byte cp.async copies from the
+// producer's lanes were measured slower, alone and beside the bulk copies.)
+//
+// Compute.  Four consumer warps form, per stage, S = Q K^T with warp-level
+// bf16 MMAs (fp32 accumulation; each warp holds a quarter of the 576 query
+// columns in registers and the four partial S tiles are summed through
+// shared memory), an online softmax, and O += P V with P kept in registers.
+//
+// Merge.  The C partial results (unnormalised O, row maximum and sum) are
+// merged through distributed shared memory, each CTA producing 512/C of
+// the value columns, in a fixed order.
+//
+// The work is bound by the gathered bytes (about 30 flops per byte at 16
+// heads), so the kernel is built around keeping the gather busy: two CTAs
+// per SM, and a split count chosen so that the grid covers the GPU once.
 #include <algorithm>
 #include <cstdint>
 #include <mutex>

@@ -23,8 +23,9 @@
 // share of the selection indices.  Before the leader has decided anything
 // each warp predicts which of its selections miss from the page table (a
 // position with no slot will miss) and stages those records from the mapped
-// host pool into its shared memory with cp.async, so that the host-link
-// transfer overlaps the leader's P0-P3.  After the cluster barrier it reads
+// host pool into the CTA's staging pool (shared memory, slots taken with an
+// atomic) with cp.async, so that the host-link transfer overlaps the
+// leader's P0-P3.  After the cluster barrier it reads
 // the leader's verdict through distributed shared memory: each staged record
 // goes to its victim slot with one bulk (TMA) copy, or is dropped if the
 // leader found a hit, and any miss of its share that was not staged is
@@ -33,6 +34,13 @@
 // followers store.  A cluster of one CTA does all of it in the leader, fetch
 // after P3.  A resolve that consumes a prefetch plan uses the leader's fetch
 // list instead of the prediction.
+//
+// Consecutive launches overlap: a plain resolve allows the next launch as
+// soon as it starts, and does P0-P3 and the followers' staging before the
+// previous grid has completed; it writes nothing to global memory before
+// then and keeps its decision only if its inputs are unchanged once that
+// grid has completed (the pair's resolve counter, written last by every
+// commit, the request id and the selection), deciding again otherwise.
 //
 // Victim selection without sorting: the LRU order array is kept sorted by
 // (stamp, slot).  A resolve at step t keeps the untouched slots in their old

@@ -128,3 +128,26 @@ def test_ragged_shapes_against_oracle(R, k, heads):
         for h in range(heads):
             ref = sparse_attention(rec, 1, q[r, h])[0]
             assert np.max(np.abs(got[r, h] - ref)) <= 4 * 2.0 ** -9 * vmax, (r, h)
+
+
+def test_many_heads_and_requests_sampled():
+    """64 requests x 128 heads: one split per (request, 16 heads), more CTAs
+    than fit at once; a sample of (request, head) against the oracle and the
+    whole output finite."""
+    R, k, heads = 64, 512, 128
+    w = configs.DSA_MLA.with_(n_requests=1, n_layers=1, n_positions=5000)
+    rng = np.random.default_rng(77)
+    rows = 8192
+    table = records.gen(w, 0, 0, np.arange(rows) % w.n_positions)
+    idx = np.stack([rng.choice(rows, k, replace=False) for _ in range(R)]).astype(np.int32)
+    q16 = _bf16_round(rng.standard_normal((R, heads, 576)).astype(np.float32))
+    got = _attend(torch.from_numpy(table).cuda(), rows, torch.from_numpy(idx).cuda(), q16,
+                  R, k, heads)
+    assert np.isfinite(got).all()
+    q = _bf16_to_f64(q16)
+    for r in (0, 17, 63):
+        rec = table[idx[r]]
+        vmax = np.abs(records.decode(w, rec)[:, :512]).max()
+        for h in (0, 15, 16, 77, 127):
+            ref = sparse_attention(rec, 1, q[r, h])[0]
+            assert np.max(np.abs(got[r, h] - ref)) <= 4 * 2.0 ** -9 * vmax, (r, h)

@@ -437,3 +437,42 @@ def test_interleaved_layers_without_synchronisation():
         for (r, l), p in orc.items():
             check_metadata(pool, w, l, r, p, w.steps)
             check_cache(pool, w, l, r, p.slot_pos)
+
+
+def test_more_requests_than_one_wave_back_to_back():
+    """400 requests (more clusters than the SMs hold at once) over two layers,
+    all launches enqueued back to back without synchronisation, against the
+    oracle: later waves start while earlier launches still run."""
+    w = _small(n_requests=400, n_layers=2, k=48, slots=64, n_positions=900, steps=6,
+               record_bytes=64)
+    sel = _random_trace(w, seed=21)
+    # some reuse between consecutive steps so that hits and evictions mix
+    for t in range(1, w.steps):
+        sel[t, :, :, :24] = sel[t - 1, :, :, 24:]
+        rng = np.random.default_rng(t)
+        for r in range(w.n_requests):
+            for l in range(w.n_layers):
+                keep = set(sel[t, r, l, :24].tolist())
+                fresh = [p for p in rng.permutation(w.n_positions) if p not in keep][:24]
+                sel[t, r, l, 24:] = fresh
+    orc = _oracles(w)
+    with hs.Pool.for_workload(w) as pool:
+        fill_selected(pool, w, sel)
+        dsel = torch.from_numpy(np.ascontiguousarray(sel.transpose(0, 2, 1, 3))).cuda()
+        out = torch.empty((w.steps, w.n_layers, w.n_requests, w.k), dtype=torch.int32,
+                          device="cuda")
+        torch.cuda.synchronize()
+        for t in range(w.steps):
+            for l in range(w.n_layers):
+                pool.resolve(l, dsel[t, l], out[t, l])
+        got = out.cpu().numpy()
+        for t in range(w.steps):
+            for l in range(w.n_layers):
+                for r in range(w.n_requests):
+                    rc, o, _ = orc[(r, l)].resolve(sel[t, r, l], out_base=r * w.slots)
+                    assert rc == OK and np.array_equal(got[t, l, r], o), (t, l, r)
+        for (r, l), p in list(orc.items())[::37]:
+            check_metadata(pool, w, l, r, p, w.steps)
+            check_cache(pool, w, l, r, p.slot_pos)
+        st = pool.stats()
+        assert st["status"] == 0 and st["resolves"] == w.steps * w.n_layers * w.n_requests

@@ -14,6 +14,10 @@ Passes, each on a freshly reset pool (warm-up steps first, then timed ones):
             step itself is timed with CUDA events: ``value``, and, divided
             by the launches of a step, the resolve kernel's average launch
             duration inside the graph (``roofline``).
+  continuous -- blocks of 16 consecutive steps captured as one graph, the
+            L2 flushed before each block only: the per-launch rate of
+            decode steps that follow each other (``continuous``, a
+            diagnostic beside ``value``, which keeps the flush per step).
   kernel -- the same steps launched one call at a time with events around
             every launch (``roofline.avg_launch_us_eager``, for context).
   e2e    -- the user's loop through the public API with host buffers: each
@@ -48,6 +52,7 @@ if ROOT not in sys.path:
 METRIC = ("resolves/sec and miss-fetch GB/s (fraction of measured pinned H2D BW) "
           "at 1 GB300")
 L2_FLUSH_BYTES = 256 << 20
+CONT_STEPS, CONT_BLOCKS = 16, 3
 
 # Counters of one steady-state resolve launch from an ncu capture (dsa_mla
 # shape, L_ctx cut to 16384: same batch, k, B, W), valid only for the kernel
@@ -377,6 +382,46 @@ def run_gpu(args, w, rank, world, dist_on):
     m_per_resolve = misses / resolves
     hbm_per_launch = R * hbm_bytes_per_resolve(k, B, m_per_resolve, W)
 
+    # ---- continuous pass (diagnostic, not `value`) --------------------------
+    # blocks of CONT_STEPS consecutive steps captured as one graph, L2
+    # flushed before each block only: the per-launch time of decode steps
+    # that follow each other with nothing in between
+    pool.reset()
+    for s in range(Wm):
+        flush(s)
+        step_eager(s % T, main)
+    blocks = []
+    for b in range(CONT_BLOCKS):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            for j in range(CONT_STEPS):
+                t = (Wm + b * CONT_STEPS + j) % T
+                for l in range(NL):
+                    hs.hs_resolve(pool.handle, l, R, None, dsel[t, l], k, out[l], None, cap)
+        blocks.append(g)
+    cont_ms, cont_bytes = [], 0
+    for g in blocks:
+        flush(0)
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        sb = pool.stats()
+        c0.record(main)
+        g.replay()
+        c1.record(main)
+        torch.cuda.synchronize()
+        cont_ms.append(c0.elapsed_time(c1))
+        cont_bytes += pool.stats()["fetched_bytes"] - sb["fetched_bytes"]
+    del blocks
+    cont_launches = CONT_BLOCKS * CONT_STEPS * launches_per_step
+    cont_s = sum(cont_ms) / 1e3
+    continuous = {
+        "what": f"{CONT_BLOCKS} blocks of {CONT_STEPS} consecutive steps, each block one graph "
+                "replay, L2 flushed before each block only; a diagnostic, not `value`",
+        "us_per_launch": cont_s / cont_launches * 1e6,
+        "resolves_per_s": CONT_BLOCKS * CONT_STEPS * R * NL / cont_s,
+        "miss_fetch_gbs": cont_bytes / cont_s / 1e9,
+        "frac_of_h2d": cont_bytes / cont_s / 1e9 / h2d_gbs,
+    }
+
     # ---- kernel pass (per-launch events, eager launches) ---------------------
     pool.reset()
     for s in range(Wm):
@@ -509,6 +554,7 @@ def run_gpu(args, w, rank, world, dist_on):
                     "hs_resolve per layer, D2H of the published slots) and a stream "
                     "synchronize; wall clock",
         },
+        "continuous": continuous,
         "cold_step": {
             "what": "step 0 from an empty cache (every selection misses), one graph replay, "
                     "L2 flushed; not in `value`",

@@ -13,12 +13,14 @@
 // cluster: the C CTAs of a cluster share one request and 16 of its query
 // heads, each owning a contiguous range of the request's k published rows.
 //
-// Gather.  In every CTA a producer warp moves its rows 32 at a time into a
-// two-stage shared-memory ring, one bulk copy per row (the TMA engine;
-// completion counted in bytes on the stage's mbarrier).  The rows are
-// scattered over the cache, so there is no tile to describe.  The slot
-// indices are read two stages ahead.  (16-byte cp.async copies from the
-// producer's lanes were measured slower, alone and beside the bulk copies.)
+// Gather.  In every CTA two producer warps move its rows 32 at a time into
+// a two-stage shared-memory ring, 16 rows each, one bulk copy per row (the
+// TMA engine; completion counted in bytes on the stage's mbarrier).  The
+// rows are scattered over the cache, so there is no tile to describe.  The
+// slot indices are read two stages ahead.  (A warp takes about a
+// microsecond to have 32 row copies accepted, so two warps issue faster
+// than one; 16-byte cp.async copies from a producer's lanes were measured
+// slower, alone and beside the bulk copies.)
 //
 // Compute.  Four consumer warps form, per stage, S = Q K^T with warp-level
 // bf16 MMAs (fp32 accumulation; each warp holds a quarter of the 576 query
@@ -47,7 +49,8 @@ namespace {
 namespace cg = cooperative_groups;
 
 constexpr int kConsumerWarps = 4;
-constexpr int kAttnThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
+constexpr int kProducerWarps = 2;               // each moves half of a stage's rows
+constexpr int kAttnThreads = (kConsumerWarps + kProducerWarps) * 32;
 constexpr int kStageKeys = 32;                // rows per pipeline stage
 constexpr int kStages = 2;
 constexpr int kMinSplitKeys = kStages * kStageKeys;
@@ -66,7 +69,7 @@ constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffKV = kOffQ + kGroup * kPitch;
 constexpr uint32_t kOffRed = kOffKV + kStages * kStageKeys * kPitch;
 constexpr uint32_t kRedBytes = kConsumerWarps * 32 * 16 * 4;  // four partial S tiles
-constexpr uint32_t kOffMask = kOffRed + 2 * kRedBytes;         // [kStages] valid-row masks
+constexpr uint32_t kOffMask = kOffRed + 2 * kRedBytes;         // [2][kStages] half-stage masks
 constexpr uint32_t kOffBar = kOffMask + 16;                    // full[2], empty[2], q
 constexpr uint32_t kAttnSmem = kOffBar + 8 * (2 * kStages + 1);
 static_assert(kStageKeys == 32, "one producer lane per row, one mask word per stage");
@@ -215,7 +218,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
 
     if (tid == 0) {
         for (int b = 0; b < kStages; ++b) {
-            mbar_init(full_bar(b), 1);
+            mbar_init(full_bar(b), kProducerWarps);  // one arrival (with bytes) per producer
             mbar_init(empty_bar(b), kConsumerWarps);
         }
         mbar_init(q_bar, 1);
@@ -232,14 +235,18 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         for (int i = 0; i < 4; ++i) o[nt][i] = 0.f;
     const int h0 = lane >> 2;  // C fragment rows h0 and h0 + 8
 
-    if (warp == kConsumerWarps) {
-        // ---------------- producer: one bulk copy per row ----------------
-        // the raw slot index of this lane's row in stage st (-1 past the
-        // split); it is checked only when used, so the load stays in flight
+    if (warp >= kConsumerWarps) {
+        // ---------------- producers: rows [16p, 16p + 16) of every stage ----
+        const int p_id = warp - kConsumerWarps;
+        constexpr int kHalf = kStageKeys / kProducerWarps;
+        // the raw slot index of row `lane` of this warp's half of stage st
+        // (-1 past the split); it is checked only when used, so the load
+        // stays in flight
         auto load_row = [&](int st) {
-            const int key = key0 + st * kStageKeys + lane;
+            const int key = key0 + st * kStageKeys + p_id * kHalf + lane;
             int32_t row = -1;
-            if (st < nstage && key < key1) row = __ldg(idx + (int64_t)r * k + key);
+            if (lane < kHalf && st < nstage && key < key1)
+                row = __ldg(idx + (int64_t)r * k + key);
             return row;
         };
         // Slot indices are read kStages stages ahead, each into the register
@@ -249,12 +256,14 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         int32_t rows[kStages];
 #pragma unroll
         for (int j = 0; j < kStages; ++j) rows[j] = load_row(j);
-        if (lane == 0) mbar_arrive_expect_tx(q_bar, kGroup * kRowBytes);
-        __syncwarp();
-        if (lane < kGroup)
-            bulk_row(smem_addr(q_s + lane * kPitch),
-                     q + ((int64_t)r * heads + (int64_t)g * kGroup + lane) * kRowBytes, kRowBytes,
-                     q_bar);
+        if (p_id == 0) {
+            if (lane == 0) mbar_arrive_expect_tx(q_bar, kGroup * kRowBytes);
+            __syncwarp();
+            if (lane < kGroup)
+                bulk_row(smem_addr(q_s + lane * kPitch),
+                         q + ((int64_t)r * heads + (int64_t)g * kGroup + lane) * kRowBytes,
+                         kRowBytes, q_bar);
+        }
         int issued = 0;
         for (int st0 = 0; st0 < nstage && ok; st0 += kStages) {
 #pragma unroll
@@ -272,17 +281,19 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
                 const int32_t raw = rows[b];
                 rows[b] = load_row(st + kStages);  // in flight for kStages stages
                 const bool use = raw >= 0 && (int64_t)raw < cache_rows;  // else a masked key
-                const uint32_t valid = __ballot_sync(0xFFFFFFFFu, use);
+                const uint32_t valid = __ballot_sync(0xFFFFFFFFu, use);  // lanes >= 16: 0
                 if (lane == 0) {
-                    maskw[b] = valid;
-                    mbar_arrive_expect_tx(full_bar(b), kStageKeys * kRowBytes);
+                    maskw[p_id * kStages + b] = valid;
+                    mbar_arrive_expect_tx(full_bar(b), kHalf * kRowBytes);
                 }
                 __syncwarp();
-                const void *src = use
-                                      ? static_cast<const void *>(cache + (int64_t)raw * kRowBytes)
-                                      : static_cast<const void *>(g_zero_row);
-                bulk_row(smem_addr(kv_s + (b * kStageKeys + lane) * kPitch), src, kRowBytes,
-                         full_bar(b));
+                if (lane < kHalf) {
+                    const void *src = use
+                                          ? static_cast<const void *>(cache + (int64_t)raw * kRowBytes)
+                                          : static_cast<const void *>(g_zero_row);
+                    bulk_row(smem_addr(kv_s + (b * kStageKeys + p_id * kHalf + lane) * kPitch), src,
+                             kRowBytes, full_bar(b));
+                }
                 issued = st + 1;
             }
         }
@@ -291,7 +302,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
         // them and this returns at once
         for (int st = max(0, issued - kStages); st < issued; ++st)
             if (!mbar_wait(full_bar(st % kStages), (st / kStages) & 1)) ok = false;
-        if (!mbar_wait(q_bar, 0)) ok = false;
+        if (p_id == 0 && !mbar_wait(q_bar, 0)) ok = false;
     } else {
         // ---------------- consumers ----------------
         ok = consumers_all(mbar_wait(q_bar, 0));
@@ -362,7 +373,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
             }
 
             // online softmax (base 2) over this stage's keys
-            const uint32_t valid = maskw[b];
+            const uint32_t valid = maskw[b] | (maskw[kStages + b] << (kStageKeys / kProducerWarps));
             float x0 = -INFINITY, x1 = -INFINITY;
 #pragma unroll
             for (int nt = 0; nt < 4; ++nt) {

@@ -160,3 +160,59 @@ def test_wrong_plan_still_exact():
         occ = a.slot_pos >= 0
         assert np.array_equal(a.cache[occ], b.cache[occ])
     assert sum(int(b.counters[4]) for b in pre[1:]) > 0
+
+
+def _bf16_records(vals):
+    """uint8 records of bf16 values (vals exactly representable in bf16)."""
+    v = np.ascontiguousarray(vals, np.float32)
+    u = (v.view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal((u.astype(np.uint32) << 16).view(np.float32), v)
+    return u.view(np.uint8).reshape(v.shape[0], -1)
+
+
+def test_mla_attention_closed_forms():
+    """576-element MLA records (K = all 576, V = the first 512, scores
+    q.K / sqrt(576)): closed forms independent of the oracle's code."""
+    rng = np.random.default_rng(5)
+    vals = rng.integers(-8, 9, size=(5, 576)).astype(np.float32) / 4   # exact in bf16
+    rec = _bf16_records(vals)
+    # a zero query weighs every key the same: the mean of the values
+    out = sparse_attention(rec, 1, np.zeros(576))
+    assert np.allclose(out[0], vals[:, :512].astype(np.float64).mean(0), rtol=0, atol=1e-12)
+    # identical keys: the common value, whatever the query
+    same = _bf16_records(np.repeat(vals[:1], 4, 0))
+    out = sparse_attention(same, 1, rng.standard_normal(576))
+    assert np.allclose(out[0], vals[0, :512], rtol=0, atol=1e-12)
+    # two keys whose scores differ by delta: weights 1 / (1 + e^delta) and
+    # e^delta / (1 + e^delta), with the 1/sqrt(576) = 1/24 scale applied
+    two = np.zeros((2, 576), np.float32)
+    two[0, 512] = 1.0                       # a key-only element (not part of V)
+    two[:, :512] = vals[:2, :512]
+    q = np.zeros(576)
+    q[512] = 24.0 * 1.5                     # score of key 0: 1.5, of key 1: 0
+    out = sparse_attention(_bf16_records(two), 1, q)
+    w0 = np.exp(1.5) / (1 + np.exp(1.5))
+    assert np.allclose(out[0], w0 * vals[0, :512] + (1 - w0) * vals[1, :512], rtol=0, atol=1e-12)
+
+
+def test_quest_attention_heads_are_independent():
+    """2048-element Quest token records: 8 heads of 128, K in [0, 1024) and
+    V in [1024, 2048), head-major; a query touching only head 3 leaves the
+    other heads' weights uniform."""
+    rng = np.random.default_rng(9)
+    vals = rng.integers(-4, 5, size=(3, 2048)).astype(np.float32) / 2
+    rec = _bf16_records(vals)
+    q = np.zeros((8, 128))
+    q[3, 0] = np.sqrt(128.0) * 2.0          # head 3's scores: 2 * K[:, 3*128]
+    out = sparse_attention(rec, 1, q)
+    assert out.shape == (8, 128)
+    V = vals[:, 1024:].reshape(3, 8, 128).astype(np.float64)
+    for h in range(8):
+        if h == 3:
+            s = 2.0 * vals[:, 3 * 128].astype(np.float64)
+            p = np.exp(s - s.max())
+            p /= p.sum()
+            want = p @ V[:, 3]
+        else:
+            want = V[:, h].mean(0)
+        assert np.allclose(out[h], want, rtol=0, atol=1e-12), h

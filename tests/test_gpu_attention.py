@@ -151,3 +151,28 @@ def test_many_heads_and_requests_sampled():
         for h in (0, 15, 16, 77, 127):
             ref = sparse_attention(rec, 1, q[r, h])[0]
             assert np.max(np.abs(got[r, h] - ref)) <= 4 * 2.0 ** -9 * vmax, (r, h)
+
+
+def test_closed_forms_on_the_gpu():
+    """A zero query weighs every published row the same (the mean of the
+    values, in fp32), and rows that are all the same record give that
+    record's values exactly."""
+    R, k, heads = 2, 200, 16
+    w = configs.DSA_MLA.with_(n_requests=1, n_layers=1, n_positions=5000)
+    rows = 1024
+    table = records.gen(w, 0, 0, np.arange(rows))
+    rng = np.random.default_rng(3)
+    idx = np.stack([rng.choice(rows, k, replace=False) for _ in range(R)]).astype(np.int32)
+    zero = np.zeros((R, heads, 576), np.uint16)
+    got = _attend(torch.from_numpy(table).cuda(), rows, torch.from_numpy(idx).cuda(), zero,
+                  R, k, heads)
+    for r in range(R):
+        mean = records.decode(w, table[idx[r]])[:, :512].mean(0)
+        for h in range(heads):
+            assert np.allclose(got[r, h], mean, rtol=1e-5, atol=1e-6), (r, h)
+    same = np.full((R, k), 7, np.int32)
+    q16 = _bf16_round(rng.standard_normal((R, heads, 576)).astype(np.float32))
+    got = _attend(torch.from_numpy(table).cuda(), rows, torch.from_numpy(same).cuda(), q16,
+                  R, k, heads)
+    v = records.decode(w, table[7:8])[0, :512].astype(np.float32)
+    assert np.array_equal(got, np.broadcast_to(v, got.shape))

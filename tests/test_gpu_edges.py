@@ -476,3 +476,66 @@ def test_more_requests_than_one_wave_back_to_back():
             check_cache(pool, w, l, r, p.slot_pos)
         st = pool.stats()
         assert st["status"] == 0 and st["resolves"] == w.steps * w.n_layers * w.n_requests
+
+
+def test_permuted_request_subsets_back_to_back():
+    """Random subsets and orders of the requests, every launch enqueued
+    without synchronisation: each launch decides early over pairs that the
+    launch before it may or may not be resolving."""
+    w = _small(n_requests=6, n_layers=2, steps=16)
+    sel = _random_trace(w, seed=15)
+    orc = _oracles(w)
+    rng = np.random.default_rng(12)
+    plan = []
+    for t in range(w.steps):
+        for l in range(w.n_layers):
+            plan.append((t, l, rng.permutation(w.n_requests)[: rng.integers(1, w.n_requests + 1)]))
+    with hs.Pool.for_workload(w) as pool:
+        fill_selected(pool, w, sel)
+        bufs = []
+        for t, l, ids in plan:
+            s = torch.from_numpy(np.ascontiguousarray(sel[t, ids, l])).cuda()
+            d_ids = torch.from_numpy(ids.astype(np.int32)).cuda()
+            bufs.append((s, d_ids, torch.empty((ids.size, w.k), dtype=torch.int32, device="cuda")))
+        torch.cuda.synchronize()
+        for (t, l, ids), (s, d_ids, out) in zip(plan, bufs):
+            pool.resolve(l, s, out, req_ids=d_ids)
+        for (t, l, ids), (s, d_ids, out) in zip(plan, bufs):
+            got = out.cpu().numpy()
+            for i, r in enumerate(ids):
+                rc, o, _ = orc[(r, l)].resolve(sel[t, r, l], out_base=r * w.slots)
+                assert rc == OK and np.array_equal(got[i], o), (t, l, r)
+        for (r, l), p in orc.items():
+            check_metadata(pool, w, l, r, p, int(p.t[0]))
+            check_cache(pool, w, l, r, p.slot_pos)
+
+
+def test_one_selection_buffer_rewritten_between_resolves():
+    """A single device selection buffer, rewritten by a copy kernel before
+    every resolve (the static-buffer pattern of captured graphs), with no
+    host synchronisation: each resolve sees its own step's selection."""
+    from workloads import traces
+    w = configs.DSA_MLA.with_(n_requests=3, n_layers=2, n_positions=9000, k=160, slots=320,
+                              steps=20, local_window=400)
+    sel = traces.generate(w)
+    orc = _oracles(w)
+    with hs.Pool.for_workload(w) as pool:
+        fill_selected(pool, w, sel)
+        dsel = torch.from_numpy(np.ascontiguousarray(sel.transpose(0, 2, 1, 3))).cuda()
+        static = torch.empty((w.n_requests, w.k), dtype=torch.int32, device="cuda")
+        out = torch.empty((w.steps, w.n_layers, w.n_requests, w.k), dtype=torch.int32,
+                          device="cuda")
+        torch.cuda.synchronize()
+        for t in range(w.steps):
+            for l in range(w.n_layers):
+                static.copy_(dsel[t, l])
+                pool.resolve(l, static, out[t, l])
+        got = out.cpu().numpy()
+        for t in range(w.steps):
+            for l in range(w.n_layers):
+                for r in range(w.n_requests):
+                    rc, o, _ = orc[(r, l)].resolve(sel[t, r, l], out_base=r * w.slots)
+                    assert rc == OK and np.array_equal(got[t, l, r], o), (t, l, r)
+        for (r, l), p in orc.items():
+            check_metadata(pool, w, l, r, p, w.steps)
+            check_cache(pool, w, l, r, p.slot_pos)

@@ -578,9 +578,11 @@ def run_prefetch_overlap(args, w):
     consumer over the slots it published (`--attn-heads` query heads per
     request), and a bf16 GEMM that stands in for the layer's MLP
     (`--compute-us` long).  For a layer that shares its anchor's selection,
-    prefetch ON plans its misses right after the anchor's resolve and copies
-    them on a side stream, so the copy overlaps the compute of the layers in
-    between; its own resolve then consumes the plan.  Four timings of the
+    prefetch ON plans its misses and copies them on a side stream as soon as
+    the anchor's selection is known (ahead of the anchor's resolve), so plan
+    and copy overlap the layers in between; the main stream waits for the
+    copy before the GEMM ahead of the layer's resolve, which then consumes
+    the plan.  Four timings of the
     same steps (CUDA events, L2 flushed before each step): the resolves
     alone, the compute alone, both without prefetch, both with prefetch.
     The share of the resolves' own time hidden behind the compute is
@@ -647,25 +649,32 @@ def run_prefetch_overlap(args, w):
             anc = w.anchors[l]
             if mode != "compute":
                 if l == anc:
-                    pool.resolve(l, dsel[t, l], out[l], stream=main)
                     if mode == "on":
+                        # The anchor's selection is known and the shared
+                        # layers' previous resolves and attention calls are
+                        # behind this point of the main stream: plan and copy
+                        # their misses on the side stream from here on.
+                        ready = torch.cuda.Event()
+                        ready.record(main)
+                        side.wait_event(ready)
                         for l2 in plans:
                             if w.anchors[l2] != l:
                                 continue
-                            pool.prefetch_plan(l, l2, dsel[t, l2], plans[l2], stream=main)
-                            ev = torch.cuda.Event()
-                            ev.record(main)
-                            side.wait_event(ev)
+                            pool.prefetch_plan(l, l2, dsel[t, l2], plans[l2], stream=side)
                             pool.prefetch_copy(l2, R, k, plans[l2], stream=side)
                             evs[l2] = torch.cuda.Event()
                             evs[l2].record(side)
+                    pool.resolve(l, dsel[t, l], out[l], stream=main)
                 elif mode == "on":
-                    main.wait_event(evs[l])
                     pool.resolve(l, dsel[t, l], out[l], plan=plans[l], stream=main)
                 else:
                     pool.resolve(l, dsel[t, l], out[l], stream=main)
             if mode != "resolve":
                 attention(l)
+                if mode == "on" and l + 1 in evs:
+                    # the next layer's copy completes before the GEMM ahead
+                    # of its resolve starts
+                    main.wait_event(evs[l + 1])
                 compute()
 
     results = {}
@@ -691,6 +700,7 @@ def run_prefetch_overlap(args, w):
                                                           "plan_mismatches", "status")}
     attn_res = time_attention(lambda: attention(0), flush, main, R, k, heads,
                               args.steps) if attn else None
+    kern = time_prefetch_kernels(pool, w, dsel, out, plans, flush, main, args)
     pool.close()
     alone = results["resolve"]
     hidden_off = 1.0 - (results["off"] - results["compute"]) / alone
@@ -712,7 +722,92 @@ def run_prefetch_overlap(args, w):
                         "prefetch_off": results["off"], "prefetch_on": results["on"]},
         "counters": {"off": results["off_stats"], "on": results["on_stats"]},
         "attention": attn_res,
+        "prefetch_kernels": kern,
         "steps": args.steps, "warmup": args.warmup,
+    }
+
+
+def time_prefetch_kernels(pool, w, dsel, out, plans, flush, stream, args):
+    """The plan and copy kernels of exact prefetch, each timed alone.
+
+    The same decode steps as prefetch ON, all on one stream and without the
+    compute: the anchor's resolve, then for each layer sharing its selection
+    the plan and the copy (each bracketed by CUDA events), then the shared
+    layers' resolves consuming the plans, so that the pool evolves exactly as
+    it does with prefetch.  L2 is flushed before every timed step.  The copy
+    moves m records of W bytes per request over the host link (roofline
+    against the pinned H2D ceiling measured here); the plan reads the
+    selection, slot map and LRU order of each request and writes its plan
+    entry (HBM roofline; its phases run one after another, so it is
+    latency-bound at these sizes).
+    """
+    import torch
+
+    from hierarchical_kv_cache_resolve_gb300 import hs
+
+    R, NL, k, B, W, T = w.n_requests, w.n_layers, w.k, w.slots, w.record_bytes, w.steps
+    h2d_gbs, _ = hs.hs_link_probe(1 << 30, 10, W)
+
+    def step(t, pending):
+        for l in range(NL):
+            if w.anchors[l] == l:
+                pool.resolve(l, dsel[t, l], out[l], stream=stream)
+                for l2 in plans:
+                    if w.anchors[l2] != l:
+                        continue
+                    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                    ev[0].record(stream)
+                    pool.prefetch_plan(l, l2, dsel[t, l2], plans[l2], stream=stream)
+                    ev[1].record(stream)
+                    pool.prefetch_copy(l2, R, k, plans[l2], stream=stream)
+                    ev[2].record(stream)
+                    pending.append(ev)
+            else:
+                pool.resolve(l, dsel[t, l], out[l], plan=plans[l], stream=stream)
+
+    pool.reset()
+    for s in range(args.warmup):
+        step(s % T, [])
+    torch.cuda.synchronize()
+    before = pool.stats(check=False)
+    plan_ms = copy_ms = 0.0
+    calls = 0
+    for i in range(args.steps):
+        flush(i)
+        pending = []
+        step((args.warmup + i) % T, pending)
+        torch.cuda.synchronize()
+        for e in pending:
+            plan_ms += e[0].elapsed_time(e[1])
+            copy_ms += e[1].elapsed_time(e[2])
+        calls += len(pending)
+    after = pool.stats(check=False)
+    if calls == 0:
+        return None
+    moved = after["prefetched_bytes"] - before["prefetched_bytes"]
+    planned = moved // W
+    plan_bytes = calls * (R * (4 * k + 6 * B + 16) + 16) + 8 * planned
+    peaks = load_peaks()
+    hbm = peaks.get("hbm_gbs") if peaks else None
+    plan_gbs = plan_bytes / (plan_ms / 1e3) / 1e9
+    copy_gbs = moved / (copy_ms / 1e3) / 1e9
+    return {
+        "calls": calls,
+        "requests_per_call": R,
+        "records_per_call": planned / calls,
+        "plan": {"us_per_call": plan_ms * 1e3 / calls, "kernels_per_call": 1,
+                 "algorithmic_bytes_per_call": plan_bytes / calls,
+                 "roofline": {"bound": "hbm", "achieved": plan_gbs, "peak": hbm,
+                              "unit": "GB/s", "frac": plan_gbs / hbm if hbm else None,
+                              "peak_source": ("MEASURED_PEAKS.json hbm_gbs (of measured)"
+                                              if hbm else None)}},
+        "copy": {"us_per_call": copy_ms * 1e3 / calls, "kernels_per_call": 1,
+                 "link_bytes_per_call": moved / calls,
+                 "roofline": {"bound": "link", "achieved": copy_gbs, "peak": h2d_gbs,
+                              "unit": "GB/s", "frac": copy_gbs / h2d_gbs,
+                              "peak_source": "pinned cudaMemcpyAsync H2D, 1 GiB, "
+                                             "best of 10, this run"}},
+        "l2": "flushed before every timed step",
     }
 
 
@@ -724,7 +819,7 @@ def attention_bytes(R: int, k: int, heads: int) -> int:
 
 
 def time_attention(call, flush, stream, R, k, heads, steps):
-    """CUDA-event time of one sparse attention call (both of its kernels) on
+    """CUDA-event time of one sparse attention call (one kernel) on
     `stream`, L2 flushed before every timed call; HBM roofline against the
     measured copy bandwidth."""
     import torch

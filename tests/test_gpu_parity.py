@@ -184,3 +184,85 @@ def test_dsa_mla_full_as_the_benchmark_runs_it():
         st = pool.stats()
         assert st["status"] == 0 and st["resolves"] == T * R * NL
     ex.shutdown()
+
+
+def test_tight_prefetch_scheduled_like_the_overlap_benchmark():
+    """Exact prefetch in the schedule of the overlap benchmark: at each
+    anchor the plans and copies of the layers sharing its selection run on a
+    side stream, concurrently with the anchor's resolve and with the
+    attention and GEMMs of the layers in between; the main stream waits for
+    a layer's copy before the GEMM ahead of that layer's plan-consuming
+    resolve; no host synchronisation from the first step to the last.  Every
+    step's published slots, the final metadata and cache, the counters, and
+    the attention each layer ran over its slots (bit-identical to the same
+    kernel over the host records of the selection, gathered densely)."""
+    from workloads import records
+
+    w = configs.TIGHT_PREFETCH.with_(n_requests=8, n_positions=30000, k=512, slots=512,
+                                     steps=12)
+    sel = traces.generate(w)
+    T, R, NL, k = sel.shape
+    heads = 16
+    scale = 576 ** -0.5
+    orc = OracleRun(w)
+    ex = ThreadPoolExecutor(16)
+    g = torch.Generator().manual_seed(11)
+    q = torch.randn((R, heads, 576), generator=g).to(torch.bfloat16).cuda()
+    a = torch.randn((2048, 2048), generator=g).to(torch.bfloat16).cuda()
+    with hs.Pool.for_workload(w) as pool:
+        fill_selected(pool, w, sel)
+        dsel = device_trace(sel)
+        out = torch.empty((T, NL, R, k), dtype=torch.int32, device="cuda")
+        att = torch.empty((T, NL, R, heads, 512), dtype=torch.float32, device="cuda")
+        plans = {l: torch.empty(hs.hs_plan_bytes(R, k), dtype=torch.uint8, device="cuda")
+                 for l in range(NL) if w.anchors[l] != l}
+        caches = [pool.views(l)["cache"] for l in range(NL)]
+        main, side = torch.cuda.current_stream(), torch.cuda.Stream()
+        torch.cuda.synchronize()
+        for t in range(T):
+            evs = {}
+            for l in range(NL):
+                if w.anchors[l] == l:
+                    ready = torch.cuda.Event()
+                    ready.record(main)
+                    side.wait_event(ready)
+                    for l2 in plans:
+                        if w.anchors[l2] == l:
+                            pool.prefetch_plan(l, l2, dsel[t, l2], plans[l2], stream=side)
+                            pool.prefetch_copy(l2, R, k, plans[l2], stream=side)
+                            evs[l2] = torch.cuda.Event()
+                            evs[l2].record(side)
+                    pool.resolve(l, dsel[t, l], out[t, l], stream=main)
+                else:
+                    pool.resolve(l, dsel[t, l], out[t, l], plan=plans[l], stream=main)
+                hs.hs_sparse_attention(q, caches[l], R * w.slots, out[t, l], R, k, heads,
+                                       scale, att[t, l], stream=main)
+                if l + 1 in evs:
+                    main.wait_event(evs[l + 1])
+                a @ a
+        torch.cuda.synchronize()
+        assert hs.hs_attention_status() == 0
+        got = out.cpu().numpy()
+        for t in range(T):
+            ores = _oracle_step(orc, sel[t], ex)
+            for (r, l), (o, m) in ores.items():
+                assert np.array_equal(got[t, l, r], o), (t, r, l)
+        for (r, l), p in orc.state.items():
+            check_metadata(pool, w, l, r, p, T)
+            check_cache(pool, w, l, r, p.slot_pos)
+        for l in range(NL):
+            st = pool.stats(l)
+            assert st["status"] == 0 and st["resolves"] == T * R
+            if l in plans:
+                assert st["plan_mismatches"] == 0 and st["fetched_bytes"] == 0
+                assert st["prefetched_bytes"] == st["misses"] * w.record_bytes
+        # what each layer's attention read was the selection's records
+        idx = torch.arange(R * k, dtype=torch.int32, device="cuda").reshape(R, k)
+        ref = torch.empty((R, heads, 512), dtype=torch.float32, device="cuda")
+        for t in range(T):
+            for l in range(NL):
+                host = np.concatenate([records.gen(w, r, l, sel[t, r, l]) for r in range(R)])
+                dense = torch.from_numpy(host).cuda()
+                hs.hs_sparse_attention(q, dense, R * k, idx, R, k, heads, scale, ref)
+                assert torch.equal(att[t, l].view(torch.int32), ref.view(torch.int32)), (t, l)
+    ex.shutdown()

@@ -75,8 +75,8 @@ def profiled_counters():
 # ---------------------------------------------------------------- helpers ---
 
 class L2Flush:
-    """Empties the L2 between timed iterations: a 256 MiB write (twice the
-    126 MB L2), then a 256 MiB read of a second buffer, so that the L2 holds
+    """Empties the L2 between timed iterations: a 256 MiB write (about twice
+    the L2), then a 256 MiB read of a second buffer, so that the L2 holds
     only clean lines and the timed work pays no write-back of the flush."""
 
     def __init__(self, dev):
@@ -102,6 +102,20 @@ def hbm_bytes_per_resolve(k: int, B: int, m: float, W: int) -> float:
     2B; writes published slots 4k, stamps 4k (every selected slot), slot map
     4m, page table 8m (new entry + evicted entry), LRU order 2B, records m*W."""
     return 4 * k + 4 * B + 2 * B + 4 * k + 4 * k + 4 * m + 8 * m + 2 * B + m * W
+
+
+def hbm_sector_bytes_per_resolve(k: int, B: int, m: float, W: int) -> float:
+    """The same resolve counted in 32-byte sectors, as the memory system
+    moves it: the contiguous arrays as above; every scattered 4-byte access
+    a whole sector (the page-table reads of the k selected positions with
+    which the data-moving CTAs predict the misses, the 8m page-table and 4m
+    slot-map writes); the stamp writes the sectors of the stamp array that
+    the k selected slots fall in (8 slots a sector, selected slots spread
+    over the B)."""
+    stamp_sectors = (B / 8.0) * (1.0 - (1.0 - min(k, B) / B) ** 8)
+    reads = 4 * k + 4 * B + 2 * B + 32 * k
+    writes = 4 * k + 32 * stamp_sectors + 32 * m + 64 * m + 2 * B + m * W
+    return reads + writes
 
 
 def load_peaks():
@@ -381,6 +395,7 @@ def run_gpu(args, w, rank, world, dist_on):
     link_bytes_per_launch = fetched / (K * launches_per_step)
     m_per_resolve = misses / resolves
     hbm_per_launch = R * hbm_bytes_per_resolve(k, B, m_per_resolve, W)
+    hbm_sectors_per_launch = R * hbm_sector_bytes_per_resolve(k, B, m_per_resolve, W)
 
     # ---- continuous pass (diagnostic, not `value`) --------------------------
     # blocks of CONT_STEPS consecutive steps captured as one graph, L2
@@ -544,6 +559,7 @@ def run_gpu(args, w, rank, world, dist_on):
             "traffic": prof["dram_bytes"] if prof else None,
             "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if hbm_peak else None,
             "algorithmic_bytes_per_launch": hbm_per_launch,
+            "sector_bytes_per_launch": hbm_sectors_per_launch,
         },
         "e2e": {
             "value": total_resolves / e2e_s,

@@ -571,9 +571,16 @@ def run_gpu(args, w, rank, world, dist_on):
                     "synchronize; wall clock",
         },
         "continuous": continuous,
+        "repeats": {
+            "what": "the timed steps in three consecutive groups, each as resolves/s "
+                    "(rank 0's device time)",
+            "resolves_per_s": [len(g) * R * NL / (sum(g) / 1e3)
+                               for g in np.array_split(np.array(step_ms), 3) if len(g)],
+        },
         "cold_step": {
             "what": "step 0 from an empty cache (every selection misses), one graph replay, "
                     "L2 flushed; not in `value`",
+            "resolves_per_s_with_timed_steps": R * NL * (K + 1) / (cold_ms / 1e3 + dev_s),
             "ms": cold_ms, "resolves_per_s": R * NL / (cold_ms / 1e3),
             "misses": st_cold["misses"],
             "miss_fetch_gbs": st_cold["fetched_bytes"] / (cold_ms / 1e3) / 1e9,

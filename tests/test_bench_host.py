@@ -20,6 +20,29 @@ def test_hbm_bytes_per_resolve_by_hand():
     assert bench.hbm_bytes_per_resolve(k, B, m, W) == reads + writes
 
 
+def test_hbm_sector_bytes_per_resolve_against_a_count_of_sectors():
+    import numpy as np
+    k, B, m, W = 2048, 4096, 267, 1152
+    got = bench.hbm_sector_bytes_per_resolve(k, B, m, W)
+    # stamp writes: the 32-byte sectors (8 slots each) of k distinct slots,
+    # counted on random slot sets
+    rng = np.random.default_rng(3)
+    touched = np.mean([len(np.unique(rng.choice(B, k, replace=False) // 8))
+                       for _ in range(200)])
+    reads = 4 * k + 4 * B + 2 * B + 32 * k   # + one sector per page-table read
+    writes = 4 * k + 32 * touched + 32 * m + 64 * m + 2 * B + m * W
+    assert abs(got - (reads + writes)) <= 0.002 * got
+    # with every slot selected the stamp array is written whole
+    assert bench.hbm_sector_bytes_per_resolve(B, B, 0, W) == (
+        4 * B + 4 * B + 2 * B + 32 * B + 4 * B + 4 * B + 2 * B)
+
+
+def test_attention_bytes_by_hand():
+    R, k, heads = 64, 2048, 16
+    assert bench.attention_bytes(R, k, heads) == (
+        R * k * 1152 + R * k * 4 + R * heads * 1152 + R * heads * 512 * 4)
+
+
 def test_rank_workloads_differ_only_in_seed():
     a, b = bench.rank_workload(configs.DSA_MLA, 0), bench.rank_workload(configs.DSA_MLA, 1)
     assert a.seed != b.seed

@@ -176,6 +176,7 @@ enum Hdr : int {
     H_G = 9,         // follower: predicted misses in its share
     H_NX = 10,       // follower: leader misses it did not predict
     H_NSTG = 11,     // follower: staging slots handed out (may exceed the capacity)
+    H_PSTAT = 12,    // plan-mode status bits, applied at the commit
     H_SUMS = 16,     // kWarps scan sums from here
 };
 

@@ -306,17 +306,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid < H_SUMS) hdr[tid] = 0u;
     // Everything above touched only registers and shared memory.  Global
     // inputs may be written by the previous grid in the stream: a plan
-    // resolve and a plan waits for it here.  A plain resolve starts before
-    // it completes (programmatic launch) and acts only on what it has
-    // checked after the wait: the leader decides on the pair's metadata and
-    // keeps the decision only if the pair's resolve counter (read before
-    // the metadata, moved after every commit), the request id and the
-    // selection are unchanged once the previous grid has completed, and
-    // decides again otherwise; the followers stage the records they predict
-    // to miss and check each one against the leader's selection.  Nothing
-    // is written to global memory before the wait, so a launch that
-    // overlaps the previous one stays exact.
-    const bool early = !kPlanOnly && !with_plan;
+    // waits for it here.  A resolve starts before it completes
+    // (programmatic launch) and acts only on what it has checked after the
+    // wait: the leader decides on the pair's metadata and keeps the
+    // decision only if the pair's resolve counter (read before the
+    // metadata, moved after every commit), the request id and the selection
+    // are unchanged once the previous grid has completed, and decides again
+    // otherwise; the followers of a plain resolve stage the records they
+    // predict to miss and check each one against the leader's selection.
+    // A consumed plan is read early too: it must come from a copy ordered
+    // before this launch, and a copy is never launched before the plan it
+    // replays has completed.  Nothing is written to global memory before
+    // the wait, so a launch that overlaps the previous one stays exact.
+    const bool early = !kPlanOnly;
     if (!early) grid_dependency_wait();
     allow_dependent_launch();
     if (crank == 0) copy_to_smem(sel_s, selr, 4 * k);  // independent of the request id
@@ -336,6 +338,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t a0 = 0, t0 = 0;
             if (tid == 0) {
                 hdr[H_ABORT] = 0u;
+                hdr[H_NF] = 0u;
+                hdr[H_PMISS] = 0u;
+                hdr[H_PHIT] = 0u;
+                hdr[H_PSTAT] = 0u;
                 if (!r_ok) {
                     a0 |= HS_STATUS_REQ_RANGE;
                 } else {
@@ -552,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const bool ok = ph->magic == kPlanMagic && ph->n_req == n_req && ph->k == k &&
                                     ph->layer == layer && eh[0] >= 0 && eh[0] <= k && eh[1] == r;
                     const int mp = ok ? eh[0] : 0;
-                    if (!ok && tid == 0) atomicOr(p.status, HS_STATUS_PLAN);
+                    if (!ok && tid == 0) atomicOr(&hdr[H_PSTAT], HS_STATUS_PLAN);
                     const int32_t *ppos = eh + 4;
                     const int32_t *pslot = ppos + k;
                     const int n = m > mp ? m : mp;
@@ -579,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     fslot[f] = ps;
                                 }
                             } else {
-                                atomicOr(p.status, HS_STATUS_PLAN);
+                                atomicOr(&hdr[H_PSTAT], HS_STATUS_PLAN);
                             }
                         }
                     }
@@ -625,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = tid; i < k; i += kThreads) o[i] = -1;
             }
             if (tid == 0) {
-                atomicOr(p.status, abort_bits);
+                atomicOr(p.status, abort_bits | (with_plan ? hdr[H_PSTAT] : 0u));
                 hdr[H_F] = 0u;
                 hdr[H_M] = 0u;
                 if (took_busy) atomicExch(&p.busy[pair], 0u);
@@ -807,6 +813,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (with_plan) {
                         atomicAdd(&c[CTR_PLAN_HITS], (unsigned long long)hdr[H_PHIT]);
                         atomicAdd(&c[CTR_PLAN_MISMATCH], (unsigned long long)hdr[H_PMISS]);
+                        if (hdr[H_PSTAT]) atomicOr(p.status, hdr[H_PSTAT]);
                     }
                 }
                 if (csize == 1 && F > 0) {
@@ -821,6 +828,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         } else if (with_plan) {
             // ------------- follower, plan consumed: the leader's fetch list ----
+            grid_dependency_wait();  // (passed by the leader already)
             cg::cluster_group cl = cg::this_cluster();
             const uint32_t *lh = cl.map_shared_rank(hdr, 0);
             const int F = (int)lh[H_F];

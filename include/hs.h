@@ -159,16 +159,18 @@ int hs_device_views(hs_pool *pool, int32_t layer, hs_views *out);
  *   hs_prefetch_copy: misses the plan covered are not copied again; any plan
  *   pair that is not exactly this resolve's own is re-fetched, so the result
  *   is the same with or without a plan.  16-byte aligned.
- * Without a plan the launch may start before the kernel ahead of it in
- * the stream has completed (programmatic dependent launch; hs_resolve allows
- * the next launch as soon as it starts, so consecutive resolves overlap):
- * it then reads d_req_ids, d_sel, the page table, the layer's metadata and
- * the host records early, stages predicted misses in shared memory and
- * takes its decision, but writes no global memory until that kernel has
- * completed, and keeps the decision only if the request id, all k
- * selections and the pair's resolve counter are unchanged by then (it
+ * The launch may start before the kernel ahead of it in the stream has
+ * completed (programmatic dependent launch; hs_resolve allows the next
+ * launch as soon as it starts, so consecutive resolves overlap): it then
+ * reads d_req_ids, d_sel, d_plan, the page table, the layer's metadata and
+ * the host records early, stages predicted misses in shared memory (without
+ * a plan) and takes its decision, but writes no global memory until that
+ * kernel has completed, and keeps the decision only if the request id, all
+ * k selections and the pair's resolve counter are unchanged by then (it
  * decides again otherwise).  The result is the one a launch started after
- * that kernel ended would give.
+ * that kernel ended would give.  d_plan is not checked that way: the
+ * ordering rule above (after the hs_prefetch_copy of the plan, which never
+ * starts before the plan is complete) keeps it fixed.
  * n_req == 0 enqueues nothing.  Errors: HS_ERR_INVALID_ARG (layer, n_req > R,
  * k outside [1, max_k], NULL d_sel/d_out), HS_ERR_CUDA (launch failed).
  */

@@ -216,3 +216,52 @@ def test_quest_attention_heads_are_independent():
         else:
             want = V[:, h].mean(0)
         assert np.allclose(out[h], want, rtol=0, atol=1e-12), h
+
+
+@pytest.mark.parametrize("heads", [1, 2, 4, 8])
+def test_per_head_records_closed_forms(heads):
+    """Token records of `heads` key blocks of 128 then `heads` value blocks:
+    the layout round-trips from blocks assembled by hand, and each head's
+    attention has the closed forms of plain softmax attention (zero query:
+    mean of its values; a query on one key element: the logistic weights of
+    the score gap; identical keys: the common value), with the scale given."""
+    from oracle.attention import split_kv_heads
+    rng = np.random.default_rng(10 + heads)
+    n = 3
+    Kb = rng.integers(-4, 5, size=(n, heads, 128)).astype(np.float32) / 2
+    Vb = rng.integers(-4, 5, size=(n, heads, 128)).astype(np.float32) / 2
+    rec = _bf16_records(np.concatenate([Kb.reshape(n, -1), Vb.reshape(n, -1)], axis=1))
+    K, V = split_kv_heads(rec, 1, heads)
+    assert np.array_equal(K, Kb.transpose(1, 0, 2)) and np.array_equal(V, Vb.transpose(1, 0, 2))
+    # zero query: every head averages its values
+    out = sparse_attention(rec, 1, np.zeros((heads, 128)), heads=heads)
+    assert np.allclose(out, Vb.astype(np.float64).mean(0), rtol=0, atol=1e-12)
+    # head h looks at key element 5 with weight 3 under scale 0.5: scores
+    # 1.5 * K[:, h, 5]; the other heads stay uniform
+    h = heads - 1
+    q = np.zeros((heads, 128))
+    q[h, 5] = 3.0
+    out = sparse_attention(rec, 1, q, heads=heads, scale=0.5)
+    s = 1.5 * Kb[:, h, 5].astype(np.float64)
+    p = np.exp(s - s.max())
+    p /= p.sum()
+    assert np.allclose(out[h], p @ Vb[:, h].astype(np.float64), rtol=0, atol=1e-12)
+    for g in range(heads - 1):
+        assert np.allclose(out[g], Vb[:, g].astype(np.float64).mean(0), rtol=0, atol=1e-12)
+    # identical keys in every record: the (identical) value, whatever the query
+    same = _bf16_records(np.repeat(np.concatenate([Kb[:1].reshape(1, -1),
+                                                   Vb[:1].reshape(1, -1)], axis=1), 4, 0))
+    out = sparse_attention(same, 1, rng.standard_normal((heads, 128)), heads=heads)
+    assert np.allclose(out, Vb[0], rtol=0, atol=1e-12)
+
+
+def test_per_head_layout_of_eight_heads_is_the_quest_layout():
+    """heads = 8 splits a 2048-element record exactly as the Quest reading
+    does: K in [0, 1024), V in [1024, 2048), head-major."""
+    from oracle.attention import split_kv_heads
+    rng = np.random.default_rng(12)
+    vals = rng.integers(-4, 5, size=(2, 2048)).astype(np.float32) / 2
+    K, V = split_kv_heads(_bf16_records(vals), 1, 8)
+    for h in range(8):
+        assert np.array_equal(K[h], vals[:, 128 * h:128 * (h + 1)])
+        assert np.array_equal(V[h], vals[:, 1024 + 128 * h:1024 + 128 * (h + 1)])

@@ -841,7 +841,14 @@ def attention_bytes(R: int, k: int, heads: int) -> int:
     return R * k * (1152 + 4) + R * heads * (1152 + 512 * 4)
 
 
-def time_attention(call, flush, stream, R, k, heads, steps):
+def attention_heads_bytes(R: int, k: int, heads: int) -> int:
+    """Algorithmic HBM bytes of one per-head attention call: the k gathered
+    records of heads * 512 bytes and k int32 slot indices per request, the
+    bf16 queries (128 per head) and the fp32 outputs (128 per head)."""
+    return R * k * (heads * 512 + 4) + R * heads * (128 * 2 + 128 * 4)
+
+
+def time_attention(call, flush, stream, R, k, heads, steps, nbytes=None):
     """CUDA-event time of one sparse attention call (one kernel) on
     `stream`, L2 flushed before every timed call; HBM roofline against the
     measured copy bandwidth."""
@@ -859,7 +866,8 @@ def time_attention(call, flush, stream, R, k, heads, steps):
         torch.cuda.synchronize()
         total += e0.elapsed_time(e1)
     s = total / steps / 1e3
-    nbytes = attention_bytes(R, k, heads)
+    if nbytes is None:
+        nbytes = attention_bytes(R, k, heads)
     peaks = load_peaks()
     peak = peaks.get("hbm_gbs") if peaks else None
     achieved = nbytes / s / 1e9
@@ -881,34 +889,50 @@ def run_attention(args, w):
     import torch
 
     from hierarchical_kv_cache_resolve_gb300 import hs
-    if w.record_bytes != 1152:
-        raise SystemExit("bench.py --attention: the consumer reads 576-element MLA records")
+    per_head = w.record_bytes != 1152
+    if per_head and (w.record_bytes % 512 or not 1 <= w.record_bytes // 512 <= 8):
+        raise SystemExit("bench.py --attention: the consumers read 576-element MLA records "
+                         "or token records of 1 to 8 heads of 128 (keys, then values)")
     dev = torch.device("cuda", torch.cuda.current_device())
-    R, k, B, heads = w.n_requests, w.k, w.slots, args.attn_heads
+    R, k, B = w.n_requests, w.k, w.slots
+    heads = w.record_bytes // 512 if per_head else args.attn_heads
     g = torch.Generator(device=dev)
     g.manual_seed(w.seed)
-    cache = torch.randn((R * B, 576), device=dev, generator=g).to(torch.bfloat16)
+    cache = torch.randn((R * B, w.record_bytes // 2), device=dev,
+                        generator=g).to(torch.bfloat16)
     idx = torch.stack([torch.randperm(B, device=dev, generator=g)[:k] + r * B
                        for r in range(R)]).to(torch.int32)
-    q = torch.randn((R, heads, 576), device=dev, generator=g).to(torch.bfloat16)
-    o = torch.empty((R, heads, 512), dtype=torch.float32, device=dev)
     flush = L2Flush(dev)
     main = torch.cuda.current_stream()
-    scale = 1.0 / math.sqrt(576.0)
+    if per_head:
+        q = torch.randn((R, heads, 128), device=dev, generator=g).to(torch.bfloat16)
+        o = torch.empty((R, heads, 128), dtype=torch.float32, device=dev)
+        scale = 1.0 / math.sqrt(128.0)
 
-    def call():
-        hs.hs_sparse_attention(q, cache, R * B, idx, R, k, heads, scale, o, stream=main)
+        def call():
+            hs.hs_sparse_attention_heads(q, cache, R * B, idx, R, k, heads, scale, o,
+                                         stream=main)
+    else:
+        q = torch.randn((R, heads, 576), device=dev, generator=g).to(torch.bfloat16)
+        o = torch.empty((R, heads, 512), dtype=torch.float32, device=dev)
+        scale = 1.0 / math.sqrt(576.0)
+
+        def call():
+            hs.hs_sparse_attention(q, cache, R * B, idx, R, k, heads, scale, o, stream=main)
 
     props = torch.cuda.get_device_properties(dev)
     sampler = ClockSampler(f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:"
                            f"{props.pci_device_id:02x}.0")
     sampler.start()
-    res = time_attention(call, flush, main, R, k, heads, args.steps)
+    res = time_attention(call, flush, main, R, k, heads, args.steps,
+                         nbytes=attention_heads_bytes(R, k, heads) if per_head else None)
     sampler.stop()
     status = hs.hs_attention_status()
     return {"metric": "sparse attention over published slots: gathered HBM GB/s",
             "value": res["roofline"]["achieved"], "unit": "GB/s", "higher_is_better": True,
             "config": {"workload": workload_name(w), "heads": heads,
+                       "consumer": ("hs_sparse_attention_heads (per-head token records)"
+                                    if per_head else "hs_sparse_attention (MLA records)"),
                        "l2": "flushed before every timed call"},
             "attention": res, "status": status, "clocks": sampler.summary(),
             "steps": args.steps, "warmup": 3}

@@ -19,7 +19,7 @@ CSRC = os.path.join(_PKG, "csrc")
 INCLUDE = os.path.join(_ROOT, "include")
 BUILD = os.path.join(_PKG, "_build")
 LIB = os.path.join(BUILD, "libhs.so")
-SOURCES = ("api.cu", "resolve.cu", "copy.cu", "noalloc.cu", "attention.cu")
+SOURCES = ("api.cu", "resolve.cu", "copy.cu", "noalloc.cu", "attention.cu", "attention_heads.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 _lock = threading.Lock()
@@ -126,7 +126,7 @@ class LayerState(ctypes.Structure):
 EXPORTS = ("hs_create_pool", "hs_destroy_pool", "hs_host_records", "hs_device_views",
            "hs_resolve", "hs_plan_bytes", "hs_prefetch_plan", "hs_prefetch_copy",
            "hs_stats", "hs_reset", "hs_link_probe", "hs_kernels_per_call", "hs_strerror",
-           "hs_resolve_noalloc", "hs_sparse_attention",
+           "hs_resolve_noalloc", "hs_sparse_attention", "hs_sparse_attention_heads",
            "hs_attention_status")
 
 
@@ -152,6 +152,8 @@ def _declare(lib):
                                ctypes.c_int),
         "hs_sparse_attention": ([vp, vp, i64, vp, i32, i32, i32, ctypes.c_float, vp, vp],
                                 ctypes.c_int),
+        "hs_sparse_attention_heads": ([vp, vp, i64, vp, i32, i32, i32, ctypes.c_float, vp, vp],
+                                      ctypes.c_int),
         "hs_attention_status": ([ctypes.POINTER(ctypes.c_uint32)], ctypes.c_int),
     }
     for name, (args, res) in sig.items():

@@ -297,6 +297,21 @@ int hs_sparse_attention(const void *d_q, const void *d_cache, int64_t cache_rows
     return cuda_ok(e) ? HS_OK : HS_ERR_CUDA;
 }
 
+int hs_sparse_attention_heads(const void *d_q, const void *d_cache, int64_t cache_rows,
+                              const int32_t *d_idx, int32_t n_req, int32_t k, int32_t heads,
+                              float scale, float *d_out, void *stream) {
+    auto misaligned = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
+    if (!d_q || !d_cache || !d_idx || !d_out || cache_rows < 1 || n_req < 0 || n_req > 65535 ||
+        k < 1 || heads < 1 || heads > 8 || misaligned(d_q) || misaligned(d_cache) ||
+        misaligned(d_out))
+        return HS_ERR_INVALID_ARG;
+    if (n_req == 0) return HS_OK;
+    const cudaError_t e = hs::launch_attention_heads(d_q, d_cache, cache_rows, d_idx, n_req, k,
+                                                     heads, scale, d_out,
+                                                     static_cast<cudaStream_t>(stream));
+    return cuda_ok(e) ? HS_OK : HS_ERR_CUDA;
+}
+
 int hs_attention_status(uint32_t *status) {
     if (!status) return HS_ERR_INVALID_ARG;
     if (!cuda_ok(cudaDeviceSynchronize())) return HS_ERR_CUDA;

@@ -180,7 +180,7 @@ enum Hdr : int {
     H_SUMS = 16,     // kWarps scan sums from here
 };
 
-// launchers (resolve.cu, copy.cu)
+// launchers (resolve.cu, copy.cu, attention.cu, attention_heads.cu)
 cudaError_t launch_resolve(const DevPool &p, int layer, int n_req, const int32_t *req_ids,
                            const int32_t *sel, int k, int32_t *out, const void *plan,
                            int cluster, cudaStream_t st);
@@ -194,6 +194,9 @@ cudaError_t launch_attention(const void *q, const void *cache, int64_t cache_row
                              const int32_t *idx, int n_req, int k, int heads, float scale,
                              float *out, cudaStream_t st);
 cudaError_t attention_status(uint32_t *status);
+cudaError_t launch_attention_heads(const void *q, const void *cache, int64_t cache_rows,
+                                   const int32_t *idx, int n_req, int k, int heads, float scale,
+                                   float *out, cudaStream_t st);
 cudaError_t launch_gather_probe(const uint8_t *src, uint8_t *dst, const int32_t *idx,
                                 int64_t n_rec, int W, int sm_count, cudaStream_t st);
 

@@ -159,6 +159,16 @@ def hs_sparse_attention(q, cache, cache_rows, idx, n_req, k, heads, scale, out,
            "hs_sparse_attention")
 
 
+def hs_sparse_attention_heads(q, cache, cache_rows, idx, n_req, k, heads, scale, out,
+                              stream=None) -> None:
+    """Attention of q [n_req][heads][128] bf16 over the published rows idx
+    [n_req][k] of a layer's cache of per-head token records (keys of every
+    head, then values; heads * 512 bytes); fp32 out [n_req][heads][128]."""
+    _check(_lib().hs_sparse_attention_heads(_ptr(q), _ptr(cache), cache_rows, _ptr(idx), n_req,
+                                            k, heads, scale, _ptr(out), _stream(stream)),
+           "hs_sparse_attention_heads")
+
+
 HS_ATTN_STATUS_TIMEOUT = 0x1
 
 

@@ -267,6 +267,31 @@ int hs_sparse_attention(const void *d_q, const void *d_cache, int64_t cache_rows
  * HS_ERR_INVALID_ARG (status == NULL), HS_ERR_CUDA. */
 int hs_attention_status(uint32_t *status);
 
+/*
+ * Sparse attention consumer for token records of per-head blocks (the
+ * Quest-style token records: for `heads` key-value heads of 128 dimensions,
+ * the record holds the heads' bf16 keys, head after head, then their bf16
+ * values, 512 bytes per head, so W = heads * 512).  For each of n_req
+ * requests and each head h, attention of q[i][h] (128 bf16) over the k
+ * records d_cache[d_idx[i][j]] -- the rows hs_resolve published:
+ *   out[i][h] = softmax_j(scale * q[i][h] . K_jh) V_jh     (fp32 out[n_req][heads][128]),
+ * with K_jh = elements [128h, 128h + 128) and V_jh = elements
+ * [128(heads + h), 128(heads + h) + 128) of record j.  Like hs_sparse_attention
+ * it is the consumer side of the exactness claim (notes, section 5 "Why It
+ * Is Exact").  d_q: device bf16 [n_req][heads][128]; d_cache: device rows of
+ * heads * 512 bytes, cache_rows of them; d_idx: device int32 [n_req][k]
+ * (an index outside [0, cache_rows) masks its row; a request with every
+ * row masked gets zeros); d_out: device fp32 [n_req][heads][128].  The
+ * three buffers are 16-byte aligned.  Scores and sums are fp32 over the
+ * bf16 inputs; one launch, no workspace, no waits that can time out; the
+ * split of the rows depends on (n_req, k) and the device only, so equal
+ * inputs give bit-identical outputs.  1 <= heads <= 8.  n_req == 0 enqueues
+ * nothing.  Errors: HS_ERR_INVALID_ARG, HS_ERR_CUDA.
+ */
+int hs_sparse_attention_heads(const void *d_q, const void *d_cache, int64_t cache_rows,
+                              const int32_t *d_idx, int32_t n_req, int32_t k, int32_t heads,
+                              float scale, float *d_out, void *stream);
+
 /* Kernels launched per call of hs_resolve / hs_prefetch_plan /
  * hs_prefetch_copy (for launch accounting; always 1 in this build). */
 int32_t hs_kernels_per_call(void);

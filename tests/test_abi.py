@@ -90,6 +90,20 @@ def test_attention_argument_checks(lib):
     assert lib.hs_attention_status(None) == hs.HS_ERR_INVALID_ARG
 
 
+def test_attention_heads_argument_checks(lib):
+    f = lib.hs_sparse_attention_heads
+    assert f(16, 16, 10, 16, 1, 10, 0, 1.0, 16, None) == hs.HS_ERR_INVALID_ARG   # heads
+    assert f(16, 16, 10, 16, 1, 10, 9, 1.0, 16, None) == hs.HS_ERR_INVALID_ARG
+    assert f(16, 16, 10, 16, 1, 0, 8, 1.0, 16, None) == hs.HS_ERR_INVALID_ARG    # k = 0
+    assert f(16, 16, 0, 16, 1, 10, 8, 1.0, 16, None) == hs.HS_ERR_INVALID_ARG    # no rows
+    assert f(8, 16, 10, 16, 1, 10, 8, 1.0, 16, None) == hs.HS_ERR_INVALID_ARG    # alignment
+    assert f(16, 8, 10, 16, 1, 10, 8, 1.0, 16, None) == hs.HS_ERR_INVALID_ARG
+    assert f(16, 16, 10, 16, 1, 10, 8, 1.0, 8, None) == hs.HS_ERR_INVALID_ARG
+    assert f(16, 16, 10, None, 1, 10, 8, 1.0, 16, None) == hs.HS_ERR_INVALID_ARG
+    assert f(16, 16, 10, 16, 70000, 10, 8, 1.0, 16, None) == hs.HS_ERR_INVALID_ARG
+    assert f(16, 16, 10, 16, 0, 10, 8, 1.0, 16, None) == hs.HS_OK   # n_req = 0: no-op
+
+
 def test_calls_on_null_pool_are_rejected(lib):
     v = _native.Views()
     s = _native.Stats()

@@ -43,6 +43,12 @@ def test_attention_bytes_by_hand():
         R * k * 1152 + R * k * 4 + R * heads * 1152 + R * heads * 512 * 4)
 
 
+def test_attention_heads_bytes_by_hand():
+    R, k, heads = 32, 2048, 8
+    assert bench.attention_heads_bytes(R, k, heads) == (
+        R * k * 8 * 512 + R * k * 4 + R * heads * 128 * 2 + R * heads * 128 * 4)
+
+
 def test_rank_workloads_differ_only_in_seed():
     a, b = bench.rank_workload(configs.DSA_MLA, 0), bench.rank_workload(configs.DSA_MLA, 1)
     assert a.seed != b.seed

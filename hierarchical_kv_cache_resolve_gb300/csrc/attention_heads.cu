@@ -12,8 +12,9 @@
 // row it reads its 256-byte key block and 256-byte value block with one
 // 8-byte load per lane each (four of the 128 dimensions per lane), forms
 // the score with a warp reduction and keeps an online softmax (base 2) and
-// its four output dimensions in registers.  The eight rows of a batch are
-// loaded together before any is used.  The C partial results (max, sum,
+// its four output dimensions in registers.  The slot indices are staged in
+// shared memory; rows go in batches of eight whose loads are issued
+// together, and the next batch is issued before the current one is used.  The C partial results (max, sum,
 // unnormalised output per head) are merged on chip through distributed
 // shared memory: CTA c writes output elements [c * heads * 128 / C, ...).
 //
@@ -39,6 +40,7 @@ constexpr int kMaxHeadsMH = 8;       // warps per CTA
 constexpr int kMaxSplitMH = 8;       // portable cluster size
 constexpr int kBatch = 8;            // rows whose loads are issued together
 constexpr int kMinRowsPerSplit = 64;
+constexpr int kIdxChunk = 512;       // slot indices staged in shared memory at a time
 
 __device__ __forceinline__ uint2 ld_nc_v2(const void *p) {
     uint2 v;
@@ -58,6 +60,7 @@ __global__ void __launch_bounds__(kMaxHeadsMH * 32)
     __shared__ __align__(16) float o_s[kMaxHeadsMH * kHeadDim];  // unnormalised output
     __shared__ float wts[kMaxHeadsMH][kMaxSplitMH];
     __shared__ float lsum[kMaxHeadsMH];
+    __shared__ int32_t rows_s[kIdxChunk];
 
     const int lane = threadIdx.x & 31, h = threadIdx.x >> 5;
     const int split = blockIdx.x, nsplit = gridDim.x, r = blockIdx.y;
@@ -73,13 +76,12 @@ __global__ void __launch_bounds__(kMaxHeadsMH * 32)
     float m = -INFINITY, l = 0.f;
     float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
     const int32_t *ir = idx + (int64_t)r * k;
-    for (int j0 = row0; j0 < row1; j0 += kBatch) {
-        bool use[kBatch];
-        uint2 kv[kBatch], vv[kBatch];
+
+    // issue the key and value loads of rows rows_s[b0 .. b0 + kBatch)
+    auto load = [&](int b0, int n, uint2 *kv, uint2 *vv, bool *use) {
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
-            const int j = j0 + u;
-            const int32_t row = j < row1 ? __ldg(ir + j) : -1;
+            const int32_t row = b0 + u < n ? rows_s[b0 + u] : -1;
             use[u] = row >= 0 && (int64_t)row < cache_rows;  // the same for every lane
             kv[u] = make_uint2(0u, 0u);
             vv[u] = make_uint2(0u, 0u);
@@ -89,6 +91,9 @@ __global__ void __launch_bounds__(kMaxHeadsMH * 32)
                 vv[u] = ld_nc_v2(rec + voff);
             }
         }
+    };
+    // scores, online softmax (base 2) and output update for one batch
+    auto consume = [&](const uint2 *kv, const uint2 *vv, const bool *use) {
         float s[kBatch];
 #pragma unroll
         for (int u = 0; u < kBatch; ++u)
@@ -105,24 +110,44 @@ __global__ void __launch_bounds__(kMaxHeadsMH * 32)
                 s[u] *= scale_log2;
                 mx = fmaxf(mx, s[u]);
             }
-        if (mx == -INFINITY) continue;  // nothing in this batch or before it
-        const float corr = exp2f(m - mx);
-        l *= corr;
-        o0 *= corr;
-        o1 *= corr;
-        o2 *= corr;
-        o3 *= corr;
+        if (mx != -INFINITY) {  // else nothing in this batch or before it
+            const float corr = exp2f(m - mx);
+            l *= corr;
+            o0 *= corr;
+            o1 *= corr;
+            o2 *= corr;
+            o3 *= corr;
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u)
-            if (use[u]) {
-                const float p = exp2f(s[u] - mx);
-                l += p;
-                o0 += p * bf_lo(vv[u].x);
-                o1 += p * bf_hi(vv[u].x);
-                o2 += p * bf_lo(vv[u].y);
-                o3 += p * bf_hi(vv[u].y);
-            }
-        m = mx;
+            for (int u = 0; u < kBatch; ++u)
+                if (use[u]) {
+                    const float p = exp2f(s[u] - mx);
+                    l += p;
+                    o0 += p * bf_lo(vv[u].x);
+                    o1 += p * bf_hi(vv[u].x);
+                    o2 += p * bf_lo(vv[u].y);
+                    o3 += p * bf_hi(vv[u].y);
+                }
+            m = mx;
+        }
+    };
+
+    // the rows in chunks of kIdxChunk slot indices staged in shared memory;
+    // within a chunk two batches alternate, each one's loads in flight while
+    // the other is consumed
+    for (int c0 = row0; c0 < row1; c0 += kIdxChunk) {
+        const int n = min(kIdxChunk, row1 - c0);
+        __syncthreads();  // the previous chunk's indices are no longer read
+        for (int i = threadIdx.x; i < n; i += blockDim.x) rows_s[i] = __ldg(ir + c0 + i);
+        __syncthreads();
+        uint2 ka[kBatch], va[kBatch], kb[kBatch], vb[kBatch];
+        bool ua[kBatch], ub[kBatch];
+        load(0, n, ka, va, ua);
+        for (int b0 = 0; b0 < n; b0 += 2 * kBatch) {
+            load(b0 + kBatch, n, kb, vb, ub);
+            consume(ka, va, ua);
+            load(b0 + 2 * kBatch, n, ka, va, ua);
+            consume(kb, vb, ub);
+        }
     }
     if (h < heads) {
         *reinterpret_cast<float4 *>(o_s + h * kHeadDim + 4 * lane) = make_float4(o0, o1, o2, o3);
@@ -171,11 +196,12 @@ __global__ void __launch_bounds__(kMaxHeadsMH * 32)
 }
 
 // Splits per request: a power of two up to 8, at least 64 rows each, and no
-// more CTAs than four per SM over the whole grid.
+// more CTAs than two per SM over the whole grid (the register budget of a
+// 256-thread CTA allows two), so that the grid is one wave.
 int nsplit_heads(int n_req, int k, int sms) {
     int c = 1;
     while (c < kMaxSplitMH && (int64_t)(2 * c) * kMinRowsPerSplit <= k &&
-           (int64_t)n_req * 2 * c <= 4 * (int64_t)sms)
+           (int64_t)n_req * 2 * c <= 2 * (int64_t)sms)
         c <<= 1;
     return c;
 }

@@ -8,11 +8,13 @@
 // positions read from the host pool.
 //
 // Work split: one thread-block cluster per request; its C CTAs split the k
-// published rows into C contiguous ranges.  Warp w of a CTA is head w: per
-// row it reads its 256-byte key block and 256-byte value block with one
-// 8-byte load per lane each (four of the 128 dimensions per lane), forms
-// the score with a warp reduction and keeps an online softmax (base 2) and
-// its four output dimensions in registers.  The slot indices are staged in
+// published rows into C contiguous ranges.  Warp w of a CTA is head w, and
+// its two half-warps take every other row: per row a half-warp reads the
+// head's 256-byte key block and 256-byte value block with one 16-byte load
+// per lane each (eight of the 128 dimensions per lane), forms the score
+// with a 16-lane reduction (one shuffle serves both halves' rows) and keeps
+// an online softmax (base 2) and its eight output dimensions in registers;
+// the two halves are combined at the end.  The slot indices are staged in
 // shared memory; rows go in batches of eight whose loads are issued
 // together, and the next batch is issued before the current one is used.  The C partial results (max, sum,
 // unnormalised output per head) are merged on chip through distributed
@@ -42,9 +44,11 @@ constexpr int kBatch = 8;            // rows whose loads are issued together
 constexpr int kMinRowsPerSplit = 64;
 constexpr int kIdxChunk = 512;       // slot indices staged in shared memory at a time
 
-__device__ __forceinline__ uint2 ld_nc_v2(const void *p) {
-    uint2 v;
-    asm("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+__device__ __forceinline__ uint4 ld_nc_v4(const void *p) {
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
     return v;
 }
 
@@ -67,65 +71,84 @@ __global__ void __launch_bounds__(kMaxHeadsMH * 32)
     const int row0 = split * split_rows;
     const int row1 = min(k, row0 + split_rows);
     const int64_t W = (int64_t)heads * 4 * kHeadDim;  // bytes per record
-    const int koff = h * 2 * kHeadDim + lane * 8;
-    const int voff = (heads + h) * 2 * kHeadDim + lane * 8;
+    // each half-warp takes every other row: lane (half, hl) holds dimensions
+    // [8 hl, 8 hl + 8) of head h for the rows of its half
+    const int half = lane >> 4, hl = lane & 15;
+    const int koff = h * 2 * kHeadDim + hl * 16;
+    const int voff = (heads + h) * 2 * kHeadDim + hl * 16;
 
-    const uint2 qr = *reinterpret_cast<const uint2 *>(q + (((int64_t)r * heads + h) * kHeadDim + 4 * lane) * 2);
-    const float q0 = bf_lo(qr.x), q1 = bf_hi(qr.x), q2 = bf_lo(qr.y), q3 = bf_hi(qr.y);
+    float qf[8];
+    {
+        const uint4 qr = *reinterpret_cast<const uint4 *>(
+            q + (((int64_t)r * heads + h) * kHeadDim + 8 * hl) * 2);
+        qf[0] = bf_lo(qr.x); qf[1] = bf_hi(qr.x); qf[2] = bf_lo(qr.y); qf[3] = bf_hi(qr.y);
+        qf[4] = bf_lo(qr.z); qf[5] = bf_hi(qr.z); qf[6] = bf_lo(qr.w); qf[7] = bf_hi(qr.w);
+    }
 
-    float m = -INFINITY, l = 0.f;
-    float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
-    const int32_t *ir = idx + (int64_t)r * k;
-
-    // issue the key and value loads of rows rows_s[b0 .. b0 + kBatch)
-    auto load = [&](int b0, int n, uint2 *kv, uint2 *vv, bool *use) {
+    float m = -INFINITY, l = 0.f;  // of this half's rows
+    float o[8];
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            const int32_t row = b0 + u < n ? rows_s[b0 + u] : -1;
-            use[u] = row >= 0 && (int64_t)row < cache_rows;  // the same for every lane
-            kv[u] = make_uint2(0u, 0u);
-            vv[u] = make_uint2(0u, 0u);
-            if (use[u]) {
+    for (int d = 0; d < 8; ++d) o[d] = 0.f;
+    const int32_t *ir = idx + (int64_t)r * k;
+    constexpr int kPairs = kBatch / 2;  // rows per half in a batch
+
+    // issue the loads of rows rows_s[b0 + 2p + half], p < kPairs
+    auto load = [&](int b0, int n, uint4 *kv, uint4 *vv, bool *use) {
+#pragma unroll
+        for (int p2 = 0; p2 < kPairs; ++p2) {
+            const int j = b0 + 2 * p2 + half;
+            const int32_t row = j < n ? rows_s[j] : -1;
+            use[p2] = row >= 0 && (int64_t)row < cache_rows;  // the same within a half
+            kv[p2] = make_uint4(0u, 0u, 0u, 0u);
+            vv[p2] = make_uint4(0u, 0u, 0u, 0u);
+            if (use[p2]) {
                 const uint8_t *rec = cache + (int64_t)row * W;
-                kv[u] = ld_nc_v2(rec + koff);
-                vv[u] = ld_nc_v2(rec + voff);
+                kv[p2] = ld_nc_v4(rec + koff);
+                vv[p2] = ld_nc_v4(rec + voff);
             }
         }
     };
-    // scores, online softmax (base 2) and output update for one batch
-    auto consume = [&](const uint2 *kv, const uint2 *vv, const bool *use) {
-        float s[kBatch];
+    // scores (a 16-lane reduction serves both halves' rows), online softmax
+    // (base 2) and output update of this half for one batch
+    auto consume = [&](const uint4 *kv, const uint4 *vv, const bool *use) {
+        float s[kPairs];
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u)
-            s[u] = q0 * bf_lo(kv[u].x) + q1 * bf_hi(kv[u].x) + q2 * bf_lo(kv[u].y) +
-                   q3 * bf_hi(kv[u].y);
+        for (int p2 = 0; p2 < kPairs; ++p2) {
+            const uint4 x = kv[p2];
+            s[p2] = qf[0] * bf_lo(x.x) + qf[1] * bf_hi(x.x) + qf[2] * bf_lo(x.y) +
+                    qf[3] * bf_hi(x.y) + qf[4] * bf_lo(x.z) + qf[5] * bf_hi(x.z) +
+                    qf[6] * bf_lo(x.w) + qf[7] * bf_hi(x.w);
+        }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
+        for (int off = 8; off > 0; off >>= 1)
 #pragma unroll
-            for (int u = 0; u < kBatch; ++u) s[u] += __shfl_xor_sync(0xFFFFFFFFu, s[u], off);
+            for (int p2 = 0; p2 < kPairs; ++p2) s[p2] += __shfl_xor_sync(0xFFFFFFFFu, s[p2], off);
         float mx = m;
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u)
-            if (use[u]) {
-                s[u] *= scale_log2;
-                mx = fmaxf(mx, s[u]);
+        for (int p2 = 0; p2 < kPairs; ++p2)
+            if (use[p2]) {
+                s[p2] *= scale_log2;
+                mx = fmaxf(mx, s[p2]);
             }
-        if (mx != -INFINITY) {  // else nothing in this batch or before it
+        if (mx != -INFINITY) {  // else nothing of this half in this batch or before it
             const float corr = exp2f(m - mx);
             l *= corr;
-            o0 *= corr;
-            o1 *= corr;
-            o2 *= corr;
-            o3 *= corr;
 #pragma unroll
-            for (int u = 0; u < kBatch; ++u)
-                if (use[u]) {
-                    const float p = exp2f(s[u] - mx);
+            for (int d = 0; d < 8; ++d) o[d] *= corr;
+#pragma unroll
+            for (int p2 = 0; p2 < kPairs; ++p2)
+                if (use[p2]) {
+                    const float p = exp2f(s[p2] - mx);
+                    const uint4 x = vv[p2];
                     l += p;
-                    o0 += p * bf_lo(vv[u].x);
-                    o1 += p * bf_hi(vv[u].x);
-                    o2 += p * bf_lo(vv[u].y);
-                    o3 += p * bf_hi(vv[u].y);
+                    o[0] += p * bf_lo(x.x);
+                    o[1] += p * bf_hi(x.x);
+                    o[2] += p * bf_lo(x.y);
+                    o[3] += p * bf_hi(x.y);
+                    o[4] += p * bf_lo(x.z);
+                    o[5] += p * bf_hi(x.z);
+                    o[6] += p * bf_lo(x.w);
+                    o[7] += p * bf_hi(x.w);
                 }
             m = mx;
         }
@@ -139,8 +162,8 @@ __global__ void __launch_bounds__(kMaxHeadsMH * 32)
         __syncthreads();  // the previous chunk's indices are no longer read
         for (int i = threadIdx.x; i < n; i += blockDim.x) rows_s[i] = __ldg(ir + c0 + i);
         __syncthreads();
-        uint2 ka[kBatch], va[kBatch], kb[kBatch], vb[kBatch];
-        bool ua[kBatch], ub[kBatch];
+        uint4 ka[kPairs], va[kPairs], kb[kPairs], vb[kPairs];
+        bool ua[kPairs], ub[kPairs];
         load(0, n, ka, va, ua);
         for (int b0 = 0; b0 < n; b0 += 2 * kBatch) {
             load(b0 + kBatch, n, kb, vb, ub);
@@ -149,9 +172,32 @@ __global__ void __launch_bounds__(kMaxHeadsMH * 32)
             consume(kb, vb, ub);
         }
     }
-    if (h < heads) {
-        *reinterpret_cast<float4 *>(o_s + h * kHeadDim + 4 * lane) = make_float4(o0, o1, o2, o3);
-        if (lane == 0) ml_s[h] = make_float2(m, l);
+
+    // the two halves' states of each head combined (lane hl and lane hl + 16
+    // hold the same dimensions)
+    {
+        const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, 16);
+        const float l2 = __shfl_xor_sync(0xFFFFFFFFu, l, 16);
+        const float M = fmaxf(m, m2);
+        const float w1 = m == -INFINITY ? 0.f : exp2f(m - M);
+        const float w2 = m2 == -INFINITY ? 0.f : exp2f(m2 - M);
+        // the sums in half order, the same on both halves
+        const float a1 = half == 0 ? w1 : w2, a2 = half == 0 ? w2 : w1;
+        const float la = half == 0 ? l : l2, lb = half == 0 ? l2 : l;
+        const float L = la * a1 + lb * a2;
+#pragma unroll
+        for (int d = 0; d < 8; ++d) {
+            const float other = __shfl_xor_sync(0xFFFFFFFFu, o[d], 16);
+            const float oa = half == 0 ? o[d] : other, ob = half == 0 ? other : o[d];
+            o[d] = oa * a1 + ob * a2;
+        }
+        if (half == 0) {
+            *reinterpret_cast<float4 *>(o_s + h * kHeadDim + 8 * hl) =
+                make_float4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<float4 *>(o_s + h * kHeadDim + 8 * hl + 4) =
+                make_float4(o[4], o[5], o[6], o[7]);
+            if (hl == 0) ml_s[h] = make_float2(M, L);
+        }
     }
     cluster.sync();  // every split's partial result is visible to the cluster
 

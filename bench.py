@@ -57,8 +57,8 @@ CONT_STEPS, CONT_BLOCKS = 16, 3
 # Counters of one steady-state resolve launch from an ncu capture (dsa_mla
 # shape, L_ctx cut to 16384: same batch, k, B, W), valid only for the kernel
 # sources they were taken on: reported as null once those sources change.
-PROFILED_SOURCES = {"resolve.cu": "5969faa6566a9b98", "hs_internal.cuh": "cb9a4c9c3ba4f2bf"}
-PROFILED_LAUNCH = {"dram_bytes": 870_656, "link_bytes": 2_073_600,
+PROFILED_SOURCES = {"resolve.cu": "5969faa6566a9b98", "hs_internal.cuh": "a609866f73457959"}
+PROFILED_LAUNCH = {"dram_bytes": 875_008, "link_bytes": 2_073_600,
                    "algorithmic_link_bytes": 2_073_600}
 
 

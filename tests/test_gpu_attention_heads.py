@@ -143,3 +143,47 @@ def test_heads_closed_forms_on_the_gpu():
     want = _bf16_to_f64(vals[0])[heads * 128:].reshape(heads, 128)
     for r in range(R):
         assert np.array_equal(got[r], want.astype(np.float32)), r
+
+
+def test_quest_decode_steps_with_the_per_head_consumer():
+    """Decode steps of the Quest page process: every layer's resolve, then the
+    per-head consumer over the slots it published, no host synchronisation
+    until the end.  Every step's published slots against the oracle, and
+    every step's attention bit-identical to the same kernel over the host
+    records of the selection gathered densely."""
+    from tests.gpu_harness import OracleRun, device_trace
+    from workloads import traces
+    w = configs.QUEST_PAGES.with_(n_requests=4, n_layers=2, n_positions=8192, k=512,
+                                  slots=1024, steps=10)
+    sel = traces.generate(w)                     # [T][R][N_l][k]
+    T, R, NL, k = sel.shape
+    heads = 8
+    rng = np.random.default_rng(31)
+    q16 = _bf16_round(rng.standard_normal((R, heads, 128)).astype(np.float32))
+    q = torch.from_numpy(q16.view(np.int16)).cuda()
+    orc = OracleRun(w)
+    with hs.Pool.for_workload(w) as pool:
+        fill_selected(pool, w, sel)
+        dsel = device_trace(sel)                  # [T][N_l][R][k]
+        out = torch.empty((T, NL, R, k), dtype=torch.int32, device="cuda")
+        att = torch.empty((T, NL, R, heads, 128), dtype=torch.float32, device="cuda")
+        caches = [pool.views(l)["cache"] for l in range(NL)]
+        torch.cuda.synchronize()
+        for t in range(T):
+            for l in range(NL):
+                pool.resolve(l, dsel[t, l], out[t, l])
+                hs.hs_sparse_attention_heads(q, caches[l], caches[l].shape[0], out[t, l], R, k,
+                                             heads, SCALE, att[t, l])
+        got = out.cpu().numpy()
+        for t in range(T):
+            for (r, l), (o, m) in orc.step(sel[t]).items():
+                assert np.array_equal(got[t, l, r], o), (t, r, l)
+        idx = torch.arange(R * k, dtype=torch.int32, device="cuda").reshape(R, k)
+        ref = torch.empty((R, heads, 128), dtype=torch.float32, device="cuda")
+        for t in range(T):
+            for l in range(NL):
+                host = np.concatenate([records.gen(w, r, l, sel[t, r, l]) for r in range(R)])
+                dense = torch.from_numpy(host).cuda()
+                hs.hs_sparse_attention_heads(q, dense, R * k, idx, R, k, heads, SCALE, ref)
+                assert torch.equal(att[t, l].view(torch.int32), ref.view(torch.int32)), (t, l)
+        assert pool.stats()["status"] == 0

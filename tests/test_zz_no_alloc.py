@@ -60,11 +60,20 @@ def test_noalloc_matches_pool_resolve_on_two_calls():
         status = torch.zeros(1, dtype=torch.int32, device="cuda")
         out_pool = torch.empty((R, k), dtype=torch.int32, device="cuda")
         out_free = torch.full((R, k), -7, dtype=torch.int32, device="cuda")
+        sels = [torch.from_numpy(np.ascontiguousarray(sel[t, :, 0])).cuda() for t in range(2)]
         for t in range(2):
-            s = torch.from_numpy(np.ascontiguousarray(sel[t, :, 0])).cuda()
+            s = sels[t]
             pool.resolve(0, s, out_pool)
+            torch.cuda.synchronize()
+            if t == 1:
+                # the first call has done the one-time set-up; the second must
+                # not change the device's free memory or torch's reserve
+                free0, reserved0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_reserved()
             hs.hs_resolve_noalloc(state, R, None, s, k, out_free, status)
             torch.cuda.synchronize()
+            if t == 1:
+                assert torch.cuda.mem_get_info()[0] == free0
+                assert torch.cuda.memory_reserved() == reserved0
             assert torch.equal(out_pool, out_free), t
             v = pool.views(0)
             assert np.array_equal(v["page_table"].cpu().numpy(), state["page_table"].cpu().numpy())
@@ -87,6 +96,23 @@ def test_noalloc_matches_pool_resolve_on_two_calls():
         torch.cuda.synchronize()
         assert int(status.item()) & hs.HS_STATUS_POS_DUP
         assert (out_free[2] == -1).all()
+
+        # misaligned caller pointers: refused before anything is enqueued
+        # (the kernel's 16-, 4- and 2-byte accesses would fault on them)
+        before = out_free.clone()
+        for name, shift in (("cache", 8), ("host_records", 4), ("page_table", 2),
+                            ("stamps", 1), ("lru", 1)):
+            base = state[name]
+            addr = base if isinstance(base, int) else base.data_ptr()
+            with pytest.raises(hs.HsError) as e:
+                hs.hs_resolve_noalloc(dict(state, **{name: addr + shift}), R, None, s, k,
+                                      out_free, status)
+            assert e.value.code == hs.HS_ERR_INVALID_ARG, name
+        with pytest.raises(hs.HsError) as e:
+            hs.hs_resolve_noalloc(state, R, None, s, k, out_free.data_ptr() + 2, status)
+        assert e.value.code == hs.HS_ERR_INVALID_ARG
+        torch.cuda.synchronize()
+        assert torch.equal(out_free, before)
 
         # more requests than the scratch array holds: refused before any launch
         big = dict(state, n_requests=hs.HS_NOALLOC_MAX_REQUESTS + 1)

@@ -19,7 +19,8 @@ CSRC = os.path.join(_PKG, "csrc")
 INCLUDE = os.path.join(_ROOT, "include")
 BUILD = os.path.join(_PKG, "_build")
 LIB = os.path.join(BUILD, "libhs.so")
-SOURCES = ("api.cu", "resolve.cu", "copy.cu", "noalloc.cu", "attention.cu", "attention_heads.cu")
+SOURCES = ("api.cu", "hostmem.cu", "resolve.cu", "copy.cu", "noalloc.cu", "attention.cu",
+           "attention_heads.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 _lock = threading.Lock()
@@ -98,7 +99,16 @@ class PoolDesc(ctypes.Structure):
     _fields_ = [("n_requests", ctypes.c_int32), ("n_layers", ctypes.c_int32),
                 ("n_positions", ctypes.c_int64), ("record_bytes", ctypes.c_int32),
                 ("slots", ctypes.c_int32), ("max_k", ctypes.c_int32),
-                ("layer_anchor", ctypes.c_void_p), ("host_limit_bytes", ctypes.c_uint64)]
+                ("layer_anchor", ctypes.c_void_p), ("host_limit_bytes", ctypes.c_uint64),
+                ("host_alloc", ctypes.c_int32)]
+
+
+class PoolInfo(ctypes.Structure):
+    _fields_ = [("host_alloc", ctypes.c_int32), ("device", ctypes.c_int32),
+                ("device_numa", ctypes.c_int32), ("host_numa_first", ctypes.c_int32),
+                ("host_numa_last", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("host_bytes", ctypes.c_uint64), ("host_mapped_bytes", ctypes.c_uint64),
+                ("host_granularity", ctypes.c_uint64), ("device_bytes", ctypes.c_uint64)]
 
 
 class Stats(ctypes.Structure):
@@ -124,7 +134,9 @@ class LayerState(ctypes.Structure):
 
 
 EXPORTS = ("hs_create_pool", "hs_destroy_pool", "hs_host_records", "hs_device_views",
-           "hs_resolve", "hs_plan_bytes", "hs_prefetch_plan", "hs_prefetch_copy",
+           "hs_pool_info", "hs_device_host_numa",
+           "hs_resolve", "hs_resolve_anchor", "hs_resolve_measure", "hs_measure_stamp_slots", "hs_plan_bytes",
+           "hs_prefetch_plan", "hs_prefetch_copy",
            "hs_stats", "hs_reset", "hs_link_probe", "hs_kernels_per_call", "hs_strerror",
            "hs_resolve_noalloc", "hs_sparse_attention", "hs_sparse_attention_heads",
            "hs_attention_status")
@@ -138,13 +150,18 @@ def _declare(lib):
         "hs_destroy_pool": ([P], ctypes.c_int),
         "hs_host_records": ([P, i32, i32, ctypes.POINTER(vp)], ctypes.c_int),
         "hs_device_views": ([P, i32, ctypes.POINTER(Views)], ctypes.c_int),
+        "hs_pool_info": ([P, ctypes.POINTER(PoolInfo)], ctypes.c_int),
+        "hs_device_host_numa": ([i32], ctypes.c_int),
         "hs_resolve": ([P, i32, i32, vp, vp, i32, vp, vp, vp], ctypes.c_int),
+        "hs_resolve_anchor": ([P, i32, i32, vp, vp, i32, vp, vp, vp], ctypes.c_int),
+        "hs_resolve_measure": ([P, i32, i32, vp, vp, i32, vp, i32, vp, vp], ctypes.c_int),
+        "hs_measure_stamp_slots": ([], i32),
         "hs_plan_bytes": ([i32, i32], ctypes.c_size_t),
         "hs_prefetch_plan": ([P, i32, i32, i32, vp, vp, i32, vp, vp], ctypes.c_int),
         "hs_prefetch_copy": ([P, i32, i32, i32, vp, vp], ctypes.c_int),
         "hs_stats": ([P, i32, ctypes.POINTER(Stats)], ctypes.c_int),
         "hs_reset": ([P], ctypes.c_int),
-        "hs_link_probe": ([ctypes.c_size_t, i32, i32, ctypes.POINTER(ctypes.c_double),
+        "hs_link_probe": ([ctypes.c_size_t, i32, i32, i32, ctypes.POINTER(ctypes.c_double),
                            ctypes.POINTER(ctypes.c_double)], ctypes.c_int),
         "hs_kernels_per_call": ([], i32),
         "hs_strerror": ([ctypes.c_int], ctypes.c_char_p),

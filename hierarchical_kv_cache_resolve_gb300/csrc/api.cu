@@ -17,7 +17,7 @@ struct hs_pool {
     int device = 0;
     int sm_count = 0;
     int cluster_override = 0;
-    void *host = nullptr;
+    hs::HostBuffer host = {};
     size_t host_bytes = 0;
     hs::DevPool dp = {};
     size_t cache_bytes = 0, pt_bytes = 0, meta_pairs = 0;
@@ -37,9 +37,11 @@ void free_device(hs_pool *p) {
     cudaFree(p->dp.busy);
     cudaFree(p->dp.counters);
     cudaFree(p->dp.status);
-    if (p->host) cudaFreeHost(p->host);
-    p->host = nullptr;
+    hs::host_free(&p->host);
 }
+
+// The host allocation a pool or probe uses for HS_HOST_ALLOC_AUTO.
+int auto_host_alloc() { return HS_HOST_ALLOC_PINNED; }
 
 int reset_state(hs_pool *p) {
     const size_t pairs = p->meta_pairs;
@@ -71,7 +73,20 @@ bool check_common(const hs_pool *p, int32_t layer, int32_t n_req, int32_t k) {
            n_req <= p->desc.n_requests && k >= 1 && k <= p->desc.max_k;
 }
 
+// int32 arrays are read and written with 4-byte accesses
+bool misaligned4(const void *a) { return (reinterpret_cast<uintptr_t>(a) & 3u) != 0; }
+
 }  // namespace
+
+static_assert(HS_STAMP_ENTRY == hs::S_ENTRY && HS_STAMP_LOADED == hs::S_LOADED &&
+                  HS_STAMP_HASHED == hs::S_HASHED && HS_STAMP_PROBED == hs::S_PROBED &&
+                  HS_STAMP_DECIDED == hs::S_DECIDED && HS_STAMP_CHECKED == hs::S_CHECKED &&
+                  HS_STAMP_VERDICT == hs::S_VERDICT && HS_STAMP_COMMITTED == hs::S_COMMITTED &&
+                  HS_STAMP_F_ISSUE == hs::S_F_ISSUE && HS_STAMP_F_ISSUED == hs::S_F_ISSUED &&
+                  HS_STAMP_F_WAITED == hs::S_F_WAITED && HS_STAMP_F_LANDED == hs::S_F_LANDED &&
+                  HS_STAMP_F_STORED == hs::S_F_STORED && HS_STAMP_ATTEMPTS == hs::S_ATTEMPTS &&
+                  HS_STAMP_EXIT == hs::S_EXIT,
+              "stamp slots of hs.h and the kernel differ");
 
 extern "C" {
 
@@ -102,7 +117,8 @@ int hs_create_pool(const hs_pool_desc *desc, hs_pool **out) {
     const hs_pool_desc d = *desc;
     if (d.n_requests < 1 || d.n_layers < 1 || d.n_positions < 1 ||
         d.n_positions > INT32_MAX || d.record_bytes < 16 || d.record_bytes % 16 != 0 ||
-        d.slots < 1 || d.slots > 32767 || d.max_k < 1 || d.max_k > d.slots)
+        d.slots < 1 || d.slots > 32767 || d.max_k < 1 || d.max_k > d.slots ||
+        d.host_alloc < HS_HOST_ALLOC_AUTO || d.host_alloc > HS_HOST_ALLOC_VMM_NUMA)
         return HS_ERR_INVALID_ARG;
     // index arithmetic limits of the kernels (32-bit chunk counters and
     // published row indices)
@@ -147,15 +163,11 @@ int hs_create_pool(const hs_pool_desc *desc, hs_pool **out) {
     p->pt_bytes = pairs * (size_t)d.n_positions * 4;
     p->host_bytes = host_bytes;
 
-    int rc = HS_OK;
-    void *hdev = nullptr;
-    if (!cuda_ok(cudaHostAlloc(&p->host, host_bytes, cudaHostAllocMapped | cudaHostAllocPortable))) {
-        p->host = nullptr;
-        rc = HS_ERR_NOMEM;
-        goto fail;
-    }
-    if (!cuda_ok(cudaHostGetDevicePointer(&hdev, p->host, 0))) { rc = HS_ERR_CUDA; goto fail; }
-    p->dp.host = static_cast<const uint8_t *>(hdev);
+    int rc = hs::host_alloc(host_bytes, d.host_alloc ? d.host_alloc : auto_host_alloc(), dev,
+                            &p->host);
+    if (rc != HS_OK) goto fail;
+    p->desc.host_alloc = p->host.kind;
+    p->dp.host = static_cast<const uint8_t *>(p->host.dev);
     if (!cuda_ok(cudaMalloc(&p->dp.cache, p->cache_bytes)) ||
         !cuda_ok(cudaMalloc(&p->dp.pt, p->pt_bytes)) ||
         !cuda_ok(cudaMalloc(&p->dp.slot_pos, pairs * B * 4)) ||
@@ -200,7 +212,35 @@ int hs_host_records(hs_pool *pool, int32_t req, int32_t layer, void **host_ptr) 
         layer >= pool->desc.n_layers)
         return HS_ERR_INVALID_ARG;
     const size_t per = (size_t)pool->desc.n_positions * pool->desc.record_bytes;
-    *host_ptr = static_cast<uint8_t *>(pool->host) + ((size_t)req * pool->desc.n_layers + layer) * per;
+    *host_ptr = static_cast<uint8_t *>(pool->host.host) + ((size_t)req * pool->desc.n_layers + layer) * per;
+    return HS_OK;
+}
+
+int hs_device_host_numa(int32_t device) {
+    int n = 0;
+    if (cudaGetDeviceCount(&n) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    if (device < 0 || device >= n) return -1;
+    return hs::device_host_numa(device);
+}
+
+int hs_pool_info(hs_pool *pool, hs_pool_info_t *out) {
+    if (!pool || !out) return HS_ERR_INVALID_ARG;
+    std::memset(out, 0, sizeof(*out));
+    out->host_alloc = pool->host.kind;
+    out->device = pool->device;
+    out->device_numa = hs::device_host_numa(pool->device);
+    const uint8_t *h = static_cast<const uint8_t *>(pool->host.host);
+    out->host_numa_first = hs::page_numa_node(h);
+    out->host_numa_last = hs::page_numa_node(h + pool->host_bytes - 1);
+    out->host_bytes = pool->host_bytes;
+    out->host_mapped_bytes = pool->host.mapped;
+    out->host_granularity = pool->host.granularity;
+    const size_t pairs = pool->meta_pairs, B = (size_t)pool->desc.slots;
+    out->device_bytes = pool->cache_bytes + pool->pt_bytes + pairs * B * (4 + 4 + 2) + pairs * 8 +
+                        (size_t)pool->desc.n_layers * hs::CTR_COUNT * 8 + 4;
     return HS_OK;
 }
 
@@ -221,16 +261,52 @@ int hs_resolve(hs_pool *pool, int32_t layer, int32_t n_req, const int32_t *d_req
                const int32_t *d_sel, int32_t k, int32_t *d_out, const void *d_plan, void *stream) {
     if (!check_common(pool, layer, n_req, k) || !d_sel || !d_out) return HS_ERR_INVALID_ARG;
     if (d_plan && (reinterpret_cast<uintptr_t>(d_plan) & 15u)) return HS_ERR_INVALID_ARG;
+    if (misaligned4(d_sel) || misaligned4(d_out) || misaligned4(d_req_ids)) return HS_ERR_INVALID_ARG;
     if (n_req == 0) return HS_OK;
     const cudaError_t e = hs::launch_resolve(pool->dp, layer, n_req, d_req_ids, d_sel, k, d_out, d_plan,
-                                             pick_cluster(pool, n_req), static_cast<cudaStream_t>(stream));
+                                             pick_cluster(pool, n_req), static_cast<cudaStream_t>(stream),
+                                             pool->anchor[layer]);
     return cuda_ok(e) ? HS_OK : HS_ERR_CUDA;
 }
+
+int hs_resolve_anchor(hs_pool *pool, int32_t layer, int32_t n_req, const int32_t *d_req_ids,
+                      const int32_t *d_sel, int32_t k, int32_t *d_out, void *d_plan_out,
+                      void *stream) {
+    if (!check_common(pool, layer, n_req, k) || !d_sel || !d_out || !d_plan_out)
+        return HS_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(d_plan_out) & 15u) || misaligned4(d_sel) || misaligned4(d_out) ||
+        misaligned4(d_req_ids))
+        return HS_ERR_INVALID_ARG;
+    if (n_req == 0) return HS_OK;
+    const cudaError_t e = hs::launch_resolve(pool->dp, layer, n_req, d_req_ids, d_sel, k, d_out,
+                                             nullptr, pick_cluster(pool, n_req),
+                                             static_cast<cudaStream_t>(stream), -1, d_plan_out);
+    return cuda_ok(e) ? HS_OK : HS_ERR_CUDA;
+}
+
+int hs_resolve_measure(hs_pool *pool, int32_t layer, int32_t n_req, const int32_t *d_req_ids,
+                       const int32_t *d_sel, int32_t k, int32_t *d_out, int32_t flags,
+                       uint64_t *d_times, void *stream) {
+    if (!check_common(pool, layer, n_req, k) || !d_sel || !d_out) return HS_ERR_INVALID_ARG;
+    if (misaligned4(d_sel) || misaligned4(d_out) || misaligned4(d_req_ids) ||
+        (reinterpret_cast<uintptr_t>(d_times) & 7u) || (flags & ~HS_MEASURE_NO_FETCH))
+        return HS_ERR_INVALID_ARG;
+    if (n_req == 0) return HS_OK;
+    const cudaError_t e = hs::launch_resolve_measure(
+        pool->dp, layer, n_req, d_req_ids, d_sel, k, d_out, (flags & HS_MEASURE_NO_FETCH) != 0,
+        reinterpret_cast<unsigned long long *>(d_times), pick_cluster(pool, n_req),
+        static_cast<cudaStream_t>(stream));
+    return cuda_ok(e) ? HS_OK : HS_ERR_CUDA;
+}
+
+int32_t hs_measure_stamp_slots(void) { return hs::kMaxCluster * hs::kStampSlots; }
 
 int hs_prefetch_plan(hs_pool *pool, int32_t anchor_layer, int32_t target_layer, int32_t n_req,
                      const int32_t *d_req_ids, const int32_t *d_sel, int32_t k, void *d_plan,
                      void *stream) {
-    if (!check_common(pool, target_layer, n_req, k) || !d_sel || !d_plan) return HS_ERR_INVALID_ARG;
+    if (!check_common(pool, target_layer, n_req, k) || !d_sel || !d_plan ||
+        misaligned4(d_sel) || misaligned4(d_req_ids))
+        return HS_ERR_INVALID_ARG;
     if (anchor_layer < 0 || anchor_layer >= pool->desc.n_layers ||
         pool->anchor[target_layer] != anchor_layer)
         return HS_ERR_INVALID_ARG;
@@ -247,7 +323,8 @@ int hs_prefetch_copy(hs_pool *pool, int32_t target_layer, int32_t n_req, int32_t
     if (reinterpret_cast<uintptr_t>(d_plan) & 15u) return HS_ERR_INVALID_ARG;
     if (n_req == 0) return HS_OK;
     const cudaError_t e = hs::launch_prefetch_copy(pool->dp, target_layer, n_req, k, d_plan,
-                                                   pool->sm_count, static_cast<cudaStream_t>(stream));
+                                                   pool->sm_count, static_cast<cudaStream_t>(stream),
+                                                   pool->anchor[target_layer]);
     return cuda_ok(e) ? HS_OK : HS_ERR_CUDA;
 }
 
@@ -318,33 +395,40 @@ int hs_attention_status(uint32_t *status) {
     return cuda_ok(hs::attention_status(status)) ? HS_OK : HS_ERR_CUDA;
 }
 
-int hs_link_probe(size_t bytes, int32_t reps, int32_t record_bytes, double *h2d_gbs,
-                  double *gather_gbs) {
-    if (bytes < (size_t)record_bytes || reps < 1 || record_bytes < 16 || record_bytes % 16)
+int hs_link_probe(size_t bytes, int32_t reps, int32_t record_bytes, int32_t host_alloc,
+                  double *h2d_gbs, double *gather_gbs) {
+    if (bytes < (size_t)record_bytes || reps < 1 || record_bytes < 16 || record_bytes % 16 ||
+        host_alloc < HS_HOST_ALLOC_AUTO || host_alloc > HS_HOST_ALLOC_VMM_NUMA)
         return HS_ERR_INVALID_ARG;
     const int64_t n_rec = (int64_t)(bytes / (size_t)record_bytes);
     if (n_rec > INT32_MAX) return HS_ERR_INVALID_ARG;
     bytes = (size_t)n_rec * record_bytes;
+    // what one timed run moves: at most 1 GiB, gathered from all of `bytes`
+    const size_t moved_cap = (size_t)1 << 30;
+    const int64_t n_move = std::min<int64_t>(n_rec, (int64_t)(moved_cap / (size_t)record_bytes));
+    const size_t moved = (size_t)n_move * record_bytes;
     int dev = 0, sms = 0;
     if (!cuda_ok(cudaGetDevice(&dev)) ||
         !cuda_ok(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)))
         return HS_ERR_CUDA;
-    void *hsrc = nullptr, *hsrc_dev = nullptr, *ddst = nullptr;
+    hs::HostBuffer hb = {};
+    void *ddst = nullptr;
     int32_t *didx = nullptr;
     cudaStream_t st = nullptr;
     cudaEvent_t e0 = nullptr, e1 = nullptr;
-    int rc = HS_OK;
-    std::vector<int32_t> idx((size_t)n_rec);
-    if (!cuda_ok(cudaHostAlloc(&hsrc, bytes, cudaHostAllocMapped | cudaHostAllocPortable))) {
-        hsrc = nullptr;
-        return HS_ERR_NOMEM;
+    std::vector<int32_t> idx((size_t)n_move);
+    int rc = hs::host_alloc(bytes, host_alloc ? host_alloc : auto_host_alloc(), dev, &hb);
+    if (rc != HS_OK) return rc;
+    if (n_move == n_rec) {
+        for (int64_t i = 0; i < n_rec; ++i) idx[(size_t)i] = (int32_t)i;
+        std::shuffle(idx.begin(), idx.end(), std::mt19937_64(12345));
+    } else {
+        std::mt19937_64 g(12345);
+        std::uniform_int_distribution<int64_t> u(0, n_rec - 1);
+        for (auto &x : idx) x = (int32_t)u(g);
     }
-    std::memset(hsrc, 0x5A, bytes);
-    for (int64_t i = 0; i < n_rec; ++i) idx[(size_t)i] = (int32_t)i;
-    std::shuffle(idx.begin(), idx.end(), std::mt19937_64(12345));
-    if (!cuda_ok(cudaHostGetDevicePointer(&hsrc_dev, hsrc, 0)) || !cuda_ok(cudaMalloc(&ddst, bytes)) ||
-        !cuda_ok(cudaMalloc(&didx, (size_t)n_rec * 4)) ||
-        !cuda_ok(cudaMemcpy(didx, idx.data(), (size_t)n_rec * 4, cudaMemcpyHostToDevice)) ||
+    if (!cuda_ok(cudaMalloc(&ddst, moved)) || !cuda_ok(cudaMalloc(&didx, (size_t)n_move * 4)) ||
+        !cuda_ok(cudaMemcpy(didx, idx.data(), (size_t)n_move * 4, cudaMemcpyHostToDevice)) ||
         !cuda_ok(cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking)) ||
         !cuda_ok(cudaEventCreate(&e0)) || !cuda_ok(cudaEventCreate(&e1))) {
         rc = HS_ERR_CUDA;
@@ -357,9 +441,9 @@ int hs_link_probe(size_t bytes, int32_t reps, int32_t record_bytes, double *h2d_
         for (int it = 0; it < reps + 1; ++it) {  // first run is a warm-up
             cudaEventRecord(e0, st);
             cudaError_t e = which == 0
-                                ? cudaMemcpyAsync(ddst, hsrc, bytes, cudaMemcpyHostToDevice, st)
-                                : hs::launch_gather_probe(static_cast<const uint8_t *>(hsrc_dev),
-                                                          static_cast<uint8_t *>(ddst), didx, n_rec,
+                                ? cudaMemcpyAsync(ddst, hb.host, moved, cudaMemcpyHostToDevice, st)
+                                : hs::launch_gather_probe(static_cast<const uint8_t *>(hb.dev),
+                                                          static_cast<uint8_t *>(ddst), didx, n_move,
                                                           record_bytes, sms, st);
             cudaEventRecord(e1, st);
             if (!cuda_ok(e) || !cuda_ok(cudaEventSynchronize(e1))) { rc = HS_ERR_CUDA; goto done; }
@@ -367,7 +451,7 @@ int hs_link_probe(size_t bytes, int32_t reps, int32_t record_bytes, double *h2d_
             cudaEventElapsedTime(&ms, e0, e1);
             if (it > 0 && (best == 0.f || ms < best)) best = ms;
         }
-        *dst = (double)bytes / (best * 1e-3) / 1e9;
+        *dst = (double)moved / (best * 1e-3) / 1e9;
     }
 done:
     if (e0) cudaEventDestroy(e0);
@@ -375,7 +459,7 @@ done:
     if (st) cudaStreamDestroy(st);
     cudaFree(didx);
     cudaFree(ddst);
-    cudaFreeHost(hsrc);
+    hs::host_free(&hb);
     return rc;
 }
 

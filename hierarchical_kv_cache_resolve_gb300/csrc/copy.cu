@@ -26,13 +26,15 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void *p) {
 }
 
 __global__ void __launch_bounds__(kThreads)
-    prefetch_copy_kernel(DevPool p, int layer, int n_req, int k, const uint8_t *__restrict__ plan) {
+    prefetch_copy_kernel(DevPool p, int layer, int n_req, int k, const uint8_t *__restrict__ plan,
+                         int plan_layer) {
     const int i = blockIdx.y;
     const PlanHeader *ph = reinterpret_cast<const PlanHeader *>(plan);
     const int32_t *eh = reinterpret_cast<const int32_t *>(plan + 16 + (size_t)i * plan_entry_bytes(k));
     const int m = eh[0], r = eh[1];
     const bool ok = ph->magic == kPlanMagic && ph->n_req == n_req && ph->k == k &&
-                    ph->layer == layer && m >= 0 && m <= k && r >= 0 && r < p.R;
+                    (ph->layer == layer || ph->layer == plan_layer) && m >= 0 && m <= k &&
+                    r >= 0 && r < p.R;
     if (!ok) {
         if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(p.status, HS_STATUS_PLAN);
         return;
@@ -122,14 +124,14 @@ __global__ void __launch_bounds__(kThreads)
 }  // namespace
 
 cudaError_t launch_prefetch_copy(const DevPool &p, int layer, int n_req, int k, const void *plan,
-                                 int sm_count, cudaStream_t st) {
+                                 int sm_count, cudaStream_t st, int plan_layer) {
     // about two CTAs per SM in total, at least one per request row
     int x = (2 * sm_count + n_req - 1) / n_req;
     const int max_x = (k * (p.W >> 4) + kThreads - 1) / kThreads;
     if (x > max_x) x = max_x;
     if (x < 1) x = 1;
-    prefetch_copy_kernel<<<dim3(x, n_req), kThreads, 0, st>>>(p, layer, n_req, k,
-                                                            static_cast<const uint8_t *>(plan));
+    prefetch_copy_kernel<<<dim3(x, n_req), kThreads, 0, st>>>(
+        p, layer, n_req, k, static_cast<const uint8_t *>(plan), plan_layer);
     return cudaGetLastError();
 }
 

@@ -162,6 +162,34 @@ __host__ __device__ inline uint32_t resolve_smem_bytes(int B, int k, bool with_p
     return a > b ? a : b;
 }
 
+// Variants of the resolve kernel.
+enum Mode : int {
+    kModeResolve = 0,  // hs_resolve
+    kModePlan = 1,     // hs_prefetch_plan
+    kModeNoFetch = 2,  // hs_resolve_measure without the miss fetch
+};
+
+// Stage timestamps of hs_resolve_measure: slot indices of one CTA's row.
+// Leader (CTA 0 of a cluster) and followers use the slots named for them.
+constexpr int kStampSlots = 16;
+enum Stamp : int {
+    S_ENTRY = 0,      // both: first instruction
+    S_LOADED = 1,     // leader: selection, slot map and LRU order in shared memory
+    S_HASHED = 2,     // leader: validated, hash table and membership bits built
+    S_PROBED = 3,     // leader: every slot probed (hits marked)
+    S_DECIDED = 4,    // leader: misses ranked and victims chosen (decision)
+    S_CHECKED = 5,    // leader: previous grid complete, early decision checked
+    S_VERDICT = 6,    // both: past the cluster barrier that publishes the decision
+    S_COMMITTED = 7,  // leader: page table, slot map, stamps, LRU order, counter written
+    S_F_ISSUE = 8,    // follower: page-table predictions read, first staging copy issued
+    S_F_ISSUED = 9,   // follower: every staging copy issued
+    S_F_WAITED = 10,  // follower: previous grid complete
+    S_F_LANDED = 11,  // follower: staged records in shared memory
+    S_F_STORED = 12,  // follower: slot stores and unstaged fetches issued
+    S_ATTEMPTS = 13,  // leader: decisions taken (a count, not a time)
+    S_EXIT = 14,      // both: last instruction
+};
+
 // header word indices (u32 at smem + hdr)
 enum Hdr : int {
     H_ABORT = 0,     // HS_STATUS_* bits that abort this request
@@ -180,14 +208,39 @@ enum Hdr : int {
     H_SUMS = 16,     // kWarps scan sums from here
 };
 
+// Host memory the GPU reads directly (hostmem.cu).  `dev` is the device
+// address of `host` (the same address for VMM allocations).
+struct HostBuffer {
+    void *host;
+    const void *dev;
+    size_t bytes;               // requested
+    size_t mapped;              // allocated (rounded up to the granularity)
+    size_t granularity;         // VMM allocation granularity, 0 for cudaHostAlloc
+    unsigned long long handle;  // VMM allocation handle
+    int kind;                   // HS_HOST_ALLOC_PINNED or HS_HOST_ALLOC_VMM_NUMA
+    int numa;                   // node requested (VMM), -1 otherwise
+};
+int host_alloc(size_t bytes, int kind, int dev, HostBuffer *out);
+int device_host_numa(int dev);
+void host_free(HostBuffer *b);
+int page_numa_node(const void *addr);
+
 // launchers (resolve.cu, copy.cu, attention.cu, attention_heads.cu)
+// plan_layer: a consumed plan may carry this layer id besides `layer` (the
+// anchor whose resolve wrote it); plan_out: where an anchor's resolve
+// writes its own miss plan (NULL: nowhere).
 cudaError_t launch_resolve(const DevPool &p, int layer, int n_req, const int32_t *req_ids,
                            const int32_t *sel, int k, int32_t *out, const void *plan,
-                           int cluster, cudaStream_t st);
+                           int cluster, cudaStream_t st, int plan_layer = -1,
+                           void *plan_out = nullptr);
 cudaError_t launch_plan(const DevPool &p, int layer, int n_req, const int32_t *req_ids,
                         const int32_t *sel, int k, void *plan, cudaStream_t st);
+cudaError_t launch_resolve_measure(const DevPool &p, int layer, int n_req, const int32_t *req_ids,
+                                   const int32_t *sel, int k, int32_t *out, bool no_fetch,
+                                   unsigned long long *times, int cluster, cudaStream_t st);
 cudaError_t launch_prefetch_copy(const DevPool &p, int layer, int n_req, int k,
-                                 const void *plan, int sm_count, cudaStream_t st);
+                                 const void *plan, int sm_count, cudaStream_t st,
+                                 int plan_layer);
 cudaError_t launch_init_lru(uint16_t *lru, int64_t pairs, int B, cudaStream_t st);
 cudaError_t prepare_kernels(size_t max_smem);
 cudaError_t launch_attention(const void *q, const void *cache, int64_t cache_rows,

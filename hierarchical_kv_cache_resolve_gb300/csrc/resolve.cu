@@ -268,11 +268,26 @@ __device__ __forceinline__ uint32_t warp_counts_exscan(uint32_t mine, uint32_t *
     return base;
 }
 
-template <bool kPlanOnly>
+// Stage timestamps (%globaltimer, ns) of the measurement variant: thread 0
+// of every CTA writes times[(request * kMaxCluster + cta) * kStampSlots + s].
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// kMode: kModeResolve (hs_resolve), kModePlan (hs_prefetch_plan: read-only
+// decision, plan written) or kModeNoFetch (the resolve without the miss
+// fetch: every metadata step, no slot written; measurement only).
+// kStamps: the same kernel with stage timestamps (measurement only).
+template <int kMode, bool kStamps>
 __global__ void __launch_bounds__(kThreads, 1)
     resolve_kernel(DevPool p, int layer, int n_req, const int32_t *__restrict__ req_ids,
                    const int32_t *__restrict__ sel_g, int k, int32_t *__restrict__ out_g,
-                   const uint8_t *__restrict__ plan_in, uint8_t *__restrict__ plan_out) {
+                   const uint8_t *__restrict__ plan_in, uint8_t *__restrict__ plan_out,
+                   unsigned long long *__restrict__ times, int plan_layer) {
+    constexpr bool kPlanOnly = kMode == kModePlan;
+    constexpr bool kNoFetch = kMode == kModeNoFetch;
     extern __shared__ __align__(16) uint8_t smem[];
     const bool with_plan = !kPlanOnly && plan_in != nullptr;
     const SmemLayout sl = smem_layout(p.B, k, with_plan, p.L);
@@ -297,6 +312,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t crank = kPlanOnly ? 0u : cluster_ctarank();
     const uint32_t csize = kPlanOnly ? 1u : cluster_nctarank();
     const int ireq = (int)(blockIdx.x / csize);
+    unsigned long long *stamp_row =
+        kStamps ? times + ((size_t)ireq * kMaxCluster + crank) * kStampSlots : nullptr;
+    auto stamp = [&](int slot) {
+        if constexpr (kStamps) {
+            if (tid == 0) stamp_row[slot] = globaltimer();
+        }
+    };
+    stamp(S_ENTRY);
     const int B = p.B, H = sl.H, W = p.W;
     const int hshift = 33 - __ffs(H);          // 32 - log2(H)
     const int mshift = 33 - __ffs(sl.M);       // 32 - log2(M)
@@ -372,6 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             cp_async_wait_all();
             __syncthreads();  // header set, shared copies landed
+            stamp(S_LOADED);
 
             // ---------------- P1: validate, hash build, membership bits ------
             {
@@ -414,6 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (bad) atomicOr(&hdr[H_ABORT], bad);
             }
             __syncthreads();
+            stamp(S_HASHED);
 
             if (hdr[H_ABORT] == 0u) {
                 // ------------- P2: probe the slots --------------------------
@@ -453,6 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 __syncthreads();
+                stamp(S_PROBED);
 
                 // ------------- P3: misses and victims (ballot scans) --------
                 // warp w owns a contiguous block of 32*seg elements of each
@@ -556,7 +582,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int32_t *eh =
                         reinterpret_cast<const int32_t *>(plan_in + 16 + (size_t)ireq * plan_entry_bytes(k));
                     const bool ok = ph->magic == kPlanMagic && ph->n_req == n_req && ph->k == k &&
-                                    ph->layer == layer && eh[0] >= 0 && eh[0] <= k && eh[1] == r;
+                                    (ph->layer == layer || ph->layer == plan_layer) && eh[0] >= 0 &&
+                                    eh[0] <= k && eh[1] == r;
                     const int mp = ok ? eh[0] : 0;
                     if (!ok && tid == 0) atomicOr(&hdr[H_PSTAT], HS_STATUS_PLAN);
                     const int32_t *ppos = eh + 4;
@@ -597,7 +624,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncthreads();
                 }
             }
-            if (!speculative) break;
+            stamp(S_DECIDED);
+            if constexpr (kStamps) {
+                if (tid == 0) stamp_row[S_ATTEMPTS] = (unsigned long long)(attempt + 1);
+            }
+            if (!speculative) {
+                stamp(S_CHECKED);  // a decision taken after the wait stands as it is
+                break;
+            }
 
             // ---------------- the speculative decision stands only if its
             // inputs are unchanged now that the previous grid has completed
@@ -615,7 +649,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     atomicOr(&hdr[H_ABORT], HS_STATUS_REQ_BUSY);
                 }
             }
-            if (!__syncthreads_or(stale)) break;
+            if (!__syncthreads_or(stale)) {
+                stamp(S_CHECKED);
+                break;
+            }
             // decide again on what the previous grid left
             r = r_now;
             r_ok = r >= 0 && r < p.R;
@@ -661,6 +698,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             return;
         }
+    } else if (kNoFetch) {
+        // measurement variant without the fetch: the followers move nothing
+        grid_dependency_wait();
     } else if (!with_plan) {
         // ---------------- follower F0: predict misses, stage their records --
         // Warp w takes blocks of 32 consecutive share entries (w, w + 16,
@@ -700,6 +740,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0 && mask) base = atomicAdd(&hdr[H_NSTG], (uint32_t)__popc(mask));
                 int slot = (int)__shfl_sync(0xFFFFFFFFu, base, 0);
                 uint32_t staged = 0;
+                if (kStamps && blk == 0) stamp(S_F_ISSUE);
                 while (mask && slot < fl.cap) {
                     const int src = __ffs(mask) - 1;
                     mask &= mask - 1;
@@ -717,9 +758,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) sbits[blk] = staged;
             }
         }
+        stamp(S_F_ISSUED);
         // the previous grid's writes are visible from here on; a request id
         // that changed under the early reads voids this CTA's staging
         grid_dependency_wait();
+        stamp(S_F_WAITED);
         const int r_now = req_ids ? req_ids[ireq] : ireq;
         if (r_now != r) {
             r = r_now;
@@ -742,9 +785,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         else
             cluster_arrive_relaxed();
         cluster_wait();
+        stamp(S_VERDICT);
 
         if (crank == 0) {
             cluster_arrive_relaxed();  // phase B: the leader's shared memory stays valid until B
+            if (plan_out != nullptr) {
+                // an anchor's resolve also writes its miss plan -- the
+                // (position, victim) pairs it commits -- for the layers that
+                // share its selection to replay (after the previous grid)
+                int32_t *eh =
+                    reinterpret_cast<int32_t *>(plan_out + 16 + (size_t)ireq * plan_entry_bytes(k));
+                const int m = hdr[H_ABORT] == 0u ? (int)hdr[H_M] : 0;
+                if (tid == 0) {
+                    eh[0] = m;
+                    eh[1] = r;
+                    eh[2] = 0;
+                    eh[3] = 0;
+                    if (ireq == 0) {
+                        PlanHeader *ph = reinterpret_cast<PlanHeader *>(plan_out);
+                        ph->magic = kPlanMagic;
+                        ph->n_req = n_req;
+                        ph->k = k;
+                        ph->layer = layer;
+                    }
+                }
+                for (int j = tid; j < m; j += kThreads) {
+                    eh[4 + j] = mpos[j];
+                    eh[4 + k + j] = mslot[j];
+                }
+            }
             if (hdr[H_ABORT] == 0u) {
                 // ------------- P4: commit metadata, publish ------------------
                 const uint32_t t = hdr[H_T];
@@ -809,6 +878,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     atomicAdd(&c[CTR_RESOLVES], 1ull);
                     atomicAdd(&c[CTR_HITS], (unsigned long long)(k - m));
                     atomicAdd(&c[CTR_MISSES], (unsigned long long)m);
+                    if (!kNoFetch)
                     atomicAdd(&c[CTR_FETCHED], (unsigned long long)F * (unsigned long long)W);
                     if (with_plan) {
                         atomicAdd(&c[CTR_PLAN_HITS], (unsigned long long)hdr[H_PHIT]);
@@ -816,7 +886,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (hdr[H_PSTAT]) atomicOr(p.status, hdr[H_PSTAT]);
                     }
                 }
-                if (csize == 1 && F > 0) {
+                stamp(S_COMMITTED);
+                if (!kNoFetch && csize == 1 && F > 0) {
                     const bool plist = hdr[H_FLIST] != 0u;
                     fetch_records(host_pair, cache_pair, plist ? fpos : mpos,
                                   plist ? fslot : mslot, F, W, tid, kThreads);
@@ -826,6 +897,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     atomicExch(&p.busy[pair], 0u);
                 }
             }
+        } else if (kNoFetch) {
+            cluster_arrive_relaxed();  // phase B: nothing to read from the leader
         } else if (with_plan) {
             // ------------- follower, plan consumed: the leader's fetch list ----
             grid_dependency_wait();  // (passed by the leader already)
@@ -901,6 +974,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             cluster_arrive_relaxed();  // phase B: done reading the leader
             cp_async_wait_all();       // no copy into shared memory outlives the CTA
             __syncthreads();           // every thread's staged copies have landed
+            stamp(S_F_LANDED);
             if (!abort) {
                 // F2: one bulk copy per staged record from shared memory to
                 // its victim slot, issued by the thread that owns the record
@@ -919,8 +993,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (nx > 0) fetch_records(host_pair, cache_pair, xp, xs, nx, W, tid, kThreads);
                 if (stored) bulk_wait_read();  // shared memory is read before the CTA ends
             }
+            if constexpr (kStamps) {
+                __syncthreads();  // (measurement variant) every thread's copies issued
+                stamp(S_F_STORED);
+            }
         }
         cluster_wait();  // phase B: no CTA leaves while the leader is being read
+        stamp(S_EXIT);
     }
 }
 
@@ -945,16 +1024,32 @@ uint32_t device_smem_optin() {
 }
 
 cudaError_t prepare_kernels(size_t max_smem) {
-    cudaError_t e = cudaFuncSetAttribute(resolve_kernel<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(resolve_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)max_smem);
+    const void *fns[] = {
+        reinterpret_cast<const void *>(resolve_kernel<kModeResolve, false>),
+        reinterpret_cast<const void *>(resolve_kernel<kModePlan, false>),
+        reinterpret_cast<const void *>(resolve_kernel<kModeResolve, true>),
+        reinterpret_cast<const void *>(resolve_kernel<kModeNoFetch, false>),
+        reinterpret_cast<const void *>(resolve_kernel<kModeNoFetch, true>),
+    };
+    for (const void *f : fns) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
-cudaError_t launch_resolve(const DevPool &p, int layer, int n_req, const int32_t *req_ids,
+namespace {
+
+// One resolve launch: a cluster of `cluster` CTAs per request, programmatic
+// stream serialisation (the launch may overlap the previous grid in the
+// stream: the kernel reads its inputs early and writes no global memory
+// before that grid has completed).
+template <int kMode, bool kStamps>
+cudaError_t launch_variant(const DevPool &p, int layer, int n_req, const int32_t *req_ids,
                            const int32_t *sel, int k, int32_t *out, const void *plan,
-                           int cluster, cudaStream_t st) {
+                           unsigned long long *times, int cluster, cudaStream_t st,
+                           int plan_layer = -1, void *plan_out = nullptr) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(n_req * cluster), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -973,22 +1068,44 @@ cudaError_t launch_resolve(const DevPool &p, int layer, int n_req, const int32_t
     attr[0].val.clusterDim.x = (unsigned)cluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    // the launch may overlap the previous grid in the stream: the kernel
-    // reads its inputs early and writes no global memory before that grid
-    // has completed
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, resolve_kernel<false>, p, layer, n_req, req_ids, sel, k, out,
-                              static_cast<const uint8_t *>(plan), static_cast<uint8_t *>(nullptr));
+    return cudaLaunchKernelEx(&cfg, resolve_kernel<kMode, kStamps>, p, layer, n_req, req_ids, sel,
+                              k, out, static_cast<const uint8_t *>(plan),
+                              static_cast<uint8_t *>(plan_out), times, plan_layer);
+}
+
+}  // namespace
+
+cudaError_t launch_resolve(const DevPool &p, int layer, int n_req, const int32_t *req_ids,
+                           const int32_t *sel, int k, int32_t *out, const void *plan,
+                           int cluster, cudaStream_t st, int plan_layer, void *plan_out) {
+    return launch_variant<kModeResolve, false>(p, layer, n_req, req_ids, sel, k, out, plan,
+                                               nullptr, cluster, st, plan_layer, plan_out);
+}
+
+cudaError_t launch_resolve_measure(const DevPool &p, int layer, int n_req, const int32_t *req_ids,
+                                   const int32_t *sel, int k, int32_t *out, bool no_fetch,
+                                   unsigned long long *times, int cluster, cudaStream_t st) {
+    if (no_fetch)
+        return times ? launch_variant<kModeNoFetch, true>(p, layer, n_req, req_ids, sel, k, out,
+                                                          nullptr, times, cluster, st)
+                     : launch_variant<kModeNoFetch, false>(p, layer, n_req, req_ids, sel, k, out,
+                                                           nullptr, nullptr, cluster, st);
+    return times ? launch_variant<kModeResolve, true>(p, layer, n_req, req_ids, sel, k, out,
+                                                      nullptr, times, cluster, st)
+                 : launch_variant<kModeResolve, false>(p, layer, n_req, req_ids, sel, k, out,
+                                                       nullptr, nullptr, cluster, st);
 }
 
 cudaError_t launch_plan(const DevPool &p, int layer, int n_req, const int32_t *req_ids,
                         const int32_t *sel, int k, void *plan, cudaStream_t st) {
     const SmemLayout sl = smem_layout(p.B, k, false, p.L);
-    resolve_kernel<true><<<n_req, kThreads, sl.total, st>>>(
-        p, layer, n_req, req_ids, sel, k, nullptr, nullptr, static_cast<uint8_t *>(plan));
+    resolve_kernel<kModePlan, false><<<n_req, kThreads, sl.total, st>>>(
+        p, layer, n_req, req_ids, sel, k, nullptr, nullptr, static_cast<uint8_t *>(plan),
+        nullptr, -1);
     return cudaGetLastError();
 }
 

@@ -25,6 +25,10 @@ HS_ERR_DEVICE_INPUT = -4
 HS_ERR_TIMEOUT = -5
 HS_ERR_UNSUPPORTED = -6
 
+HS_HOST_ALLOC_AUTO = 0
+HS_HOST_ALLOC_PINNED = 1
+HS_HOST_ALLOC_VMM_NUMA = 2
+
 HS_STATUS_POS_RANGE = 0x1
 HS_STATUS_POS_DUP = 0x2
 HS_STATUS_REQ_RANGE = 0x4
@@ -82,13 +86,13 @@ def hs_plan_bytes(n_req: int, k: int) -> int:
 
 
 def hs_create_pool(n_requests, n_layers, n_positions, record_bytes, slots, max_k,
-                   layer_anchor=None, host_limit_bytes=0) -> int:
+                   layer_anchor=None, host_limit_bytes=0, host_alloc=HS_HOST_ALLOC_AUTO) -> int:
     anchors = None
     if layer_anchor is not None:
         anchors = (ctypes.c_int32 * len(layer_anchor))(*layer_anchor)
     d = _native.PoolDesc(n_requests, n_layers, n_positions, record_bytes, slots, max_k,
                          ctypes.cast(anchors, ctypes.c_void_p) if anchors is not None else None,
-                         host_limit_bytes)
+                         host_limit_bytes, host_alloc)
     h = ctypes.c_void_p()
     _check(_lib().hs_create_pool(ctypes.byref(d), ctypes.byref(h)), "hs_create_pool")
     return h.value
@@ -110,9 +114,44 @@ def hs_device_views(pool: int, layer: int) -> _native.Views:
     return v
 
 
+def hs_device_host_numa(device: int) -> int:
+    """Host NUMA node closest to `device`, -1 when none is reported."""
+    return int(_lib().hs_device_host_numa(device))
+
+
+def hs_pool_info(pool: int) -> dict:
+    i = _native.PoolInfo()
+    _check(_lib().hs_pool_info(pool, ctypes.byref(i)), "hs_pool_info")
+    return {f: int(getattr(i, f)) for f, _ in _native.PoolInfo._fields_ if f != "reserved"}
+
+
 def hs_resolve(pool, layer, n_req, req_ids, sel, k, out, plan=None, stream=None) -> None:
     _check(_lib().hs_resolve(pool, layer, n_req, _ptr(req_ids), _ptr(sel), k, _ptr(out),
                              _ptr(plan), _stream(stream)), "hs_resolve")
+
+
+def hs_resolve_anchor(pool, layer, n_req, req_ids, sel, k, out, plan_out, stream=None) -> None:
+    _check(_lib().hs_resolve_anchor(pool, layer, n_req, _ptr(req_ids), _ptr(sel), k, _ptr(out),
+                                    _ptr(plan_out), _stream(stream)), "hs_resolve_anchor")
+
+
+HS_MEASURE_NO_FETCH = 0x1
+HS_STAMPS = ("ENTRY", "LOADED", "HASHED", "PROBED", "DECIDED", "CHECKED", "VERDICT", "COMMITTED",
+             "F_ISSUE", "F_ISSUED", "F_WAITED", "F_LANDED", "F_STORED", "ATTEMPTS", "EXIT")
+HS_STAMP = {name: i for i, name in enumerate(HS_STAMPS)}
+
+
+def hs_measure_stamp_slots() -> int:
+    return int(_lib().hs_measure_stamp_slots())
+
+
+def hs_resolve_measure(pool, layer, n_req, req_ids, sel, k, out, flags=0, times=None,
+                       stream=None) -> None:
+    """Measurement variant of hs_resolve: HS_MEASURE_NO_FETCH skips the miss
+    fetch; `times` (device u64 [n_req][hs_measure_stamp_slots()]) receives
+    stage timestamps."""
+    _check(_lib().hs_resolve_measure(pool, layer, n_req, _ptr(req_ids), _ptr(sel), k, _ptr(out),
+                                     flags, _ptr(times), _stream(stream)), "hs_resolve_measure")
 
 
 def hs_prefetch_plan(pool, anchor_layer, target_layer, n_req, req_ids, sel, k, plan,
@@ -142,11 +181,13 @@ def hs_reset(pool) -> None:
     _check(_lib().hs_reset(pool), "hs_reset")
 
 
-def hs_link_probe(nbytes: int, reps: int = 10, record_bytes: int = 1152):
-    """(H2D memcpy GB/s, scattered-record GPU-load GB/s), best of `reps`."""
+def hs_link_probe(nbytes: int, reps: int = 10, record_bytes: int = 1152,
+                  host_alloc: int = HS_HOST_ALLOC_AUTO):
+    """(H2D memcpy GB/s, scattered-record GPU-load GB/s), best of `reps`,
+    over a host buffer of `nbytes` allocated the `host_alloc` way."""
     a, b = ctypes.c_double(), ctypes.c_double()
-    _check(_lib().hs_link_probe(nbytes, reps, record_bytes, ctypes.byref(a), ctypes.byref(b)),
-           "hs_link_probe")
+    _check(_lib().hs_link_probe(nbytes, reps, record_bytes, host_alloc, ctypes.byref(a),
+                                ctypes.byref(b)), "hs_link_probe")
     return a.value, b.value
 
 
@@ -209,16 +250,19 @@ class Pool:
     """A pool handle plus host and device views."""
 
     def __init__(self, n_requests, n_layers, n_positions, record_bytes, slots, max_k,
-                 layer_anchor=None, host_limit_bytes=0):
+                 layer_anchor=None, host_limit_bytes=0, host_alloc=HS_HOST_ALLOC_AUTO):
         self.R, self.NL, self.L = n_requests, n_layers, n_positions
         self.W, self.B, self.max_k = record_bytes, slots, max_k
         self.handle = hs_create_pool(n_requests, n_layers, n_positions, record_bytes, slots,
-                                     max_k, layer_anchor, host_limit_bytes)
+                                     max_k, layer_anchor, host_limit_bytes, host_alloc)
 
     @classmethod
-    def for_workload(cls, w, host_limit_bytes=0):
+    def for_workload(cls, w, host_limit_bytes=0, host_alloc=HS_HOST_ALLOC_AUTO):
         return cls(w.n_requests, w.n_layers, w.n_positions, w.record_bytes, w.slots, w.k,
-                   list(w.anchors), host_limit_bytes)
+                   list(w.anchors), host_limit_bytes, host_alloc)
+
+    def info(self) -> dict:
+        return hs_pool_info(self.handle)
 
     def close(self):
         if self.handle:
@@ -261,6 +305,14 @@ class Pool:
     def resolve(self, layer, sel, out, req_ids=None, plan=None, stream=None, n_req=None):
         n = sel.shape[0] if n_req is None else n_req
         hs_resolve(self.handle, layer, n, req_ids, sel, sel.shape[-1], out, plan, stream)
+
+    def resolve_anchor(self, layer, sel, out, plan_out, req_ids=None, stream=None):
+        hs_resolve_anchor(self.handle, layer, sel.shape[0], req_ids, sel, sel.shape[-1], out,
+                          plan_out, stream)
+
+    def resolve_measure(self, layer, sel, out, flags=0, times=None, req_ids=None, stream=None):
+        hs_resolve_measure(self.handle, layer, sel.shape[0], req_ids, sel, sel.shape[-1], out,
+                           flags, times, stream)
 
     def prefetch_plan(self, anchor_layer, target_layer, sel, plan, req_ids=None, stream=None):
         hs_prefetch_plan(self.handle, anchor_layer, target_layer, sel.shape[0], req_ids, sel,

@@ -84,7 +84,28 @@ typedef struct {
     /* Refuse pools whose pinned host pool would exceed this many bytes
        (0: no limit beyond what the system grants).  HS_ERR_NOMEM. */
     uint64_t host_limit_bytes;
+    /* How the host pool is allocated: HS_HOST_ALLOC_* (0: the library's
+       choice, see HS_HOST_ALLOC_AUTO). */
+    int32_t host_alloc;
 } hs_pool_desc;
+
+/* ---- host pool memory (hs_pool_desc.host_alloc, hs_link_probe) --------- */
+/* The library's choice: HS_HOST_ALLOC_PINNED.  (Measured on GB300:
+ * scattered 1152-byte GPU-thread reads of cudaHostAlloc memory run at the
+ * full pinned-copy rate while the pool stays within the device's
+ * translation reach, about 16 GiB; those of VMM host-NUMA memory at about
+ * a fifth of it at any size.) */
+#define HS_HOST_ALLOC_AUTO 0
+/* cudaHostAlloc(Mapped | Portable), made while the calling thread prefers
+ * the host NUMA node closest to the device (set_mempolicy), so that the
+ * pinned pages come from that node; the device reads them through its
+ * mapping of the allocation. */
+#define HS_HOST_ALLOC_PINNED 1
+/* Virtual memory management API: one pinned host allocation on the NUMA
+ * node closest to the device (cudaDevAttrHostNumaId), mapped at a 1 GiB
+ * aligned virtual range readable and writable by the device and the host
+ * at the same address. */
+#define HS_HOST_ALLOC_VMM_NUMA 2
 
 typedef struct {
     uint64_t resolves;          /* resolves committed (one per request per call) */
@@ -139,6 +160,29 @@ int hs_host_records(hs_pool *pool, int32_t req, int32_t layer, void **host_ptr);
 /* Device views of `layer` (see hs_views). */
 int hs_device_views(hs_pool *pool, int32_t layer, hs_views *out);
 
+/* Where a pool's memory lives (for placement checks and reports). */
+typedef struct {
+    int32_t host_alloc;        /* HS_HOST_ALLOC_PINNED or HS_HOST_ALLOC_VMM_NUMA */
+    int32_t device;            /* CUDA device of the pool */
+    int32_t device_numa;       /* host NUMA node closest to that device, -1 unknown */
+    int32_t host_numa_first;   /* NUMA node of the first page of the host pool, -1 unknown */
+    int32_t host_numa_last;    /* NUMA node of its last page, -1 unknown */
+    int32_t reserved;
+    uint64_t host_bytes;       /* bytes of host records */
+    uint64_t host_mapped_bytes;/* bytes allocated for them (granularity-rounded) */
+    uint64_t host_granularity; /* VMM allocation granularity, 0 for cudaHostAlloc */
+    uint64_t device_bytes;     /* bytes of device arrays the pool allocated */
+} hs_pool_info_t;
+
+/* Fills *out.  Errors: HS_ERR_INVALID_ARG (NULL pool or out). */
+int hs_pool_info(hs_pool *pool, hs_pool_info_t *out);
+
+/* Host NUMA node closest to CUDA device `device` (cudaDevAttrHostNumaId),
+ * where a pool created on that device places its host records; -1 when
+ * the system reports none or the device does not exist.  A process serving
+ * several devices (one per rank) can bind each rank's threads to it. */
+int hs_device_host_numa(int32_t device);
+
 /*
  * RESOLVE for one sparse layer: for each of the n_req requests
  * r = d_req_ids[i] (or r = i when d_req_ids is NULL), given its k selected
@@ -153,12 +197,16 @@ int hs_device_views(hs_pool *pool, int32_t layer, hs_views *out);
  *      order, and writes d_out[i][j] = r * B + slot of d_sel[i][j].
  * (notes, section 3; Pith review, "What carries the argument".)
  * d_req_ids: device int32[n_req] or NULL; ids must be distinct.
- * d_sel: device int32[n_req][k]; d_out: device int32[n_req][k].
- * d_plan: NULL, or a plan made by hs_prefetch_plan for this layer with the
- *   same n_req, request ids, selection and k, already copied by
- *   hs_prefetch_copy: misses the plan covered are not copied again; any plan
- *   pair that is not exactly this resolve's own is re-fetched, so the result
- *   is the same with or without a plan.  16-byte aligned.
+ * d_sel: device int32[n_req][k]; d_out: device int32[n_req][k].  The three
+ *   are 4-byte aligned (HS_ERR_INVALID_ARG otherwise).
+ * d_plan: NULL, or a plan with the same n_req, request ids, selection and
+ *   k, already copied by hs_prefetch_copy into this layer: one made by
+ *   hs_prefetch_plan for this layer, or the miss plan hs_resolve_anchor
+ *   wrote when it resolved this layer's anchor.  Misses the plan covered
+ *   are not copied again; any plan pair that is not exactly this resolve's
+ *   own is re-fetched (and a slot the copy wrote for such a pair is
+ *   refilled with the record it must hold), so the result is the same with
+ *   or without a plan.  16-byte aligned.
  * The launch may start before the kernel ahead of it in the stream has
  * completed (programmatic dependent launch; hs_resolve allows the next
  * launch as soon as it starts, so consecutive resolves overlap): it then
@@ -177,6 +225,83 @@ int hs_device_views(hs_pool *pool, int32_t layer, hs_views *out);
 int hs_resolve(hs_pool *pool, int32_t layer, int32_t n_req, const int32_t *d_req_ids,
                const int32_t *d_sel, int32_t k, int32_t *d_out, const void *d_plan,
                void *stream);
+
+/*
+ * Measurement variant of hs_resolve (not for serving; it never feeds a
+ * throughput figure of hs_resolve).  Same arguments, launch shape and
+ * results as hs_resolve without a plan, with two options:
+ *   flags & HS_MEASURE_NO_FETCH: the resolve without step 4 -- hash build,
+ *     probe, victim choice, page-table / slot-map / stamp / LRU update and
+ *     publication all run, no host record is read and no slot is written.
+ *     It isolates the metadata cost, which the pages report as no
+ *     measurable per-token cost against a no-IO baseline (Pith review,
+ *     Fig. 7 "Miss-resolution breakdown" and the verdict's no-IO oracle).
+ *     Afterwards the pool's slots no longer hold the records their slot
+ *     map names: hs_reset before resolving for real.  fetched_bytes is not
+ *     counted; resolves, hits and misses are.
+ *   d_times (NULL: none): device u64[n_req][hs_measure_stamp_slots()],
+ *     8-byte aligned; each CTA of request i's cluster (at most 8) writes
+ *     %globaltimer nanosecond stamps of its stages into its row of 16
+ *     (row i * 8 + cta; slot meanings in the HS_STAMP_* list below; slots
+ *     a CTA does not reach are left as they were).
+ * Errors as hs_resolve; HS_ERR_INVALID_ARG for unknown flags or a
+ * misaligned d_times.
+ */
+#define HS_MEASURE_NO_FETCH 0x1
+/* Stamp slots: leader = CTA 0 of a request's cluster, followers = the
+ * others.  ENTRY, VERDICT (past the cluster barrier that publishes the
+ * decision) and EXIT for every CTA; LOADED (selection and slot metadata in
+ * shared memory), HASHED, PROBED, DECIDED (misses ranked, victims chosen),
+ * CHECKED (previous grid complete, early decision confirmed), COMMITTED
+ * (metadata written) for the leader; F_ISSUE (first staging copy issued),
+ * F_ISSUED (all issued), F_WAITED (previous grid complete), F_LANDED
+ * (staged records in shared memory), F_STORED (slot stores and unstaged
+ * fetches issued) for followers; ATTEMPTS holds the leader's count of
+ * decisions, not a time. */
+#define HS_STAMP_ENTRY 0
+#define HS_STAMP_LOADED 1
+#define HS_STAMP_HASHED 2
+#define HS_STAMP_PROBED 3
+#define HS_STAMP_DECIDED 4
+#define HS_STAMP_CHECKED 5
+#define HS_STAMP_VERDICT 6
+#define HS_STAMP_COMMITTED 7
+#define HS_STAMP_F_ISSUE 8
+#define HS_STAMP_F_ISSUED 9
+#define HS_STAMP_F_WAITED 10
+#define HS_STAMP_F_LANDED 11
+#define HS_STAMP_F_STORED 12
+#define HS_STAMP_ATTEMPTS 13
+#define HS_STAMP_EXIT 14
+int hs_resolve_measure(hs_pool *pool, int32_t layer, int32_t n_req, const int32_t *d_req_ids,
+                       const int32_t *d_sel, int32_t k, int32_t *d_out, int32_t flags,
+                       uint64_t *d_times, void *stream);
+
+/* u64 entries per request in hs_resolve_measure's d_times (8 CTAs x 16). */
+int32_t hs_measure_stamp_slots(void);
+
+/*
+ * hs_resolve of an anchor layer that also writes its miss plan: for every
+ * request, the (position, victim slot) pairs it commits, in the format of
+ * hs_prefetch_plan, into d_plan_out (hs_plan_bytes(n_req, k) bytes,
+ * 16-byte aligned; a rejected request gets an empty entry).  The layers
+ * that share the anchor's selection (desc.layer_anchor) and have seen the
+ * same selections since the pool was created or reset hold the same slots
+ * in the same recency order, so this is their miss plan too: the anchor's
+ * miss plan that a copy-only kernel replays into them ahead of their own
+ * resolves (notes, section 4 "Exact Layer-Wise Prefetching"; Pith review,
+ * Fig. 8) -- hs_prefetch_copy(target, d_plan_out) on a side stream, then
+ * hs_resolve(target, ..., d_plan_out), with no hs_prefetch_plan launch.
+ * A layer whose history differs stays exact through the consuming
+ * resolve's check of every pair.  The plan is written after the previous
+ * grid in the stream has completed (like every global write of the
+ * resolve); it must not be overwritten while a copy or resolve that
+ * consumes it may run.  Errors as hs_resolve, and HS_ERR_INVALID_ARG for a
+ * NULL or misaligned d_plan_out.
+ */
+int hs_resolve_anchor(hs_pool *pool, int32_t layer, int32_t n_req, const int32_t *d_req_ids,
+                      const int32_t *d_sel, int32_t k, int32_t *d_out, void *d_plan_out,
+                      void *stream);
 
 /* Bytes of a plan buffer for n_req requests of k selections. */
 size_t hs_plan_bytes(int32_t n_req, int32_t k);
@@ -199,7 +324,8 @@ int hs_prefetch_plan(hs_pool *pool, int32_t anchor_layer, int32_t target_layer,
 /*
  * Exact layer-wise prefetch, copy half: a copy-only kernel that writes
  * host[r][target_layer][pos] into slot `slot` of request r for every pair of
- * d_plan (n_req, k as given to hs_prefetch_plan).  Meant for a side stream
+ * d_plan (n_req, k as given to hs_prefetch_plan or hs_resolve_anchor; a
+ * plan of target_layer or of its anchor layer).  Meant for a side stream
  * so that the transfer overlaps other work (notes, section 4).  It touches
  * no metadata: the consuming hs_resolve commits it.
  */
@@ -219,17 +345,23 @@ int hs_stats(hs_pool *pool, int32_t layer, hs_stats_t *out);
 int hs_reset(hs_pool *pool);
 
 /*
- * Link ceiling probe (not part of the hot path).  Allocates `bytes` of
- * pinned host memory and the same on the device, then reports the best of
- * `reps` timed runs (CUDA events) of
- *   *h2d_gbs:    cudaMemcpyAsync host -> device of the whole buffer;
- *   *gather_gbs: a kernel that copies `bytes` worth of record_bytes-sized
- *                records from random record indices of the pinned buffer
- *                into device memory with 16-byte GPU-thread loads.
+ * Link ceiling probe (not part of the hot path).  Allocates `bytes` of host
+ * memory the way host_alloc says (HS_HOST_ALLOC_*), and min(bytes, 1 GiB)
+ * on the device, then reports the best of `reps` timed runs (CUDA events) of
+ *   *h2d_gbs:    cudaMemcpyAsync host -> device of min(bytes, 1 GiB) from
+ *                the start of the host buffer;
+ *   *gather_gbs: a kernel that copies min(bytes, 1 GiB) worth of
+ *                record_bytes-sized records, from record indices drawn
+ *                uniformly over the WHOLE host buffer (a permutation when
+ *                bytes <= 1 GiB), into device memory with 16-byte
+ *                GPU-thread loads -- the miss fetch's access pattern over a
+ *                pool of `bytes`.
  * Either output pointer may be NULL.  Frees what it allocated.
+ * Errors: HS_ERR_INVALID_ARG, HS_ERR_NOMEM, HS_ERR_UNSUPPORTED (the
+ * allocation kind is not available), HS_ERR_CUDA.
  */
-int hs_link_probe(size_t bytes, int32_t reps, int32_t record_bytes, double *h2d_gbs,
-                  double *gather_gbs);
+int hs_link_probe(size_t bytes, int32_t reps, int32_t record_bytes, int32_t host_alloc,
+                  double *h2d_gbs, double *gather_gbs);
 
 /*
  * Sparse attention consumer over published slots (decode).  For each of
@@ -341,6 +473,8 @@ typedef struct {
  * library until the process exits.  The first call on a device looks up
  * that array's device address (cudaGetSymbolAddress) and configures the
  * kernel; make that first call before any stream capture on the device.
+ * The address is kept per device and per context: after a device reset the
+ * next call (again outside a capture) looks it up anew in the new context.
  * Each call clears the part of the array it uses (an asynchronous memset on
  * `stream`) before launching, and every call shares the array: calls that
  * overlap on the GPU, on any streams, race.  Per-call counters are not
@@ -348,8 +482,12 @@ typedef struct {
  *
  * d_status: NULL, or a device u32 into which the kernel ORs HS_STATUS_* bits
  *   for rejected requests (never cleared by the call).
+ * Alignment: host_records and cache 16 bytes; page_table, slot_pos,
+ * stamps, resolves, d_req_ids, d_sel, d_out and d_status 4 bytes; lru 2
+ * bytes (the kernel's access widths).
  * Errors: HS_ERR_INVALID_ARG (NULL state/arrays/d_sel/d_out, fields out of
- * range, n_req > R, k outside [1, B]); HS_ERR_UNSUPPORTED (R above
+ * range, n_req > R, k outside [1, B], a misaligned pointer: refused before
+ * anything is enqueued); HS_ERR_UNSUPPORTED (R above
  * HS_NOALLOC_MAX_REQUESTS, or B and k needing more shared memory than a CTA
  * has); HS_ERR_CUDA.  No cudaMalloc, cudaFree or allocating library routine
  * is called.

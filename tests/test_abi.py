@@ -46,7 +46,7 @@ def test_host_only_helpers(lib):
 
 def _desc(**kw):
     d = dict(n_requests=2, n_layers=2, n_positions=1000, record_bytes=128, slots=64,
-             max_k=32, layer_anchor=None, host_limit_bytes=0)
+             max_k=32, layer_anchor=None, host_limit_bytes=0, host_alloc=0)
     d.update(kw)
     return _native.PoolDesc(**d)
 
@@ -54,7 +54,7 @@ def _desc(**kw):
 @pytest.mark.parametrize("bad", [
     dict(n_requests=0), dict(n_layers=0), dict(n_positions=0), dict(n_positions=1 << 31),
     dict(record_bytes=100), dict(record_bytes=0), dict(slots=0), dict(slots=40000),
-    dict(max_k=0), dict(max_k=65)])
+    dict(max_k=0), dict(max_k=65), dict(host_alloc=-1), dict(host_alloc=3)])
 def test_create_pool_rejects_bad_descriptors(lib, bad):
     h = ctypes.c_void_p(1234)
     rc = lib.hs_create_pool(ctypes.byref(_desc(**bad)), ctypes.byref(h))
@@ -116,4 +116,29 @@ def test_calls_on_null_pool_are_rejected(lib):
     assert lib.hs_host_records(None, 0, 0, ctypes.byref(p)) == hs.HS_ERR_INVALID_ARG
     assert lib.hs_reset(None) == hs.HS_ERR_INVALID_ARG
     assert lib.hs_destroy_pool(None) == hs.HS_OK
-    assert lib.hs_link_probe(8, 0, 1152, None, None) == hs.HS_ERR_INVALID_ARG
+    assert lib.hs_link_probe(8, 0, 1152, 0, None, None) == hs.HS_ERR_INVALID_ARG
+    assert lib.hs_link_probe(1 << 20, 1, 1152, 7, None, None) == hs.HS_ERR_INVALID_ARG
+    assert lib.hs_pool_info(None, None) == hs.HS_ERR_INVALID_ARG
+
+
+def test_noalloc_refuses_misaligned_pointers_before_any_cuda_call(lib):
+    """hs_resolve_noalloc checks the alignment its kernel's accesses need
+    (16-byte records and slots, 4-byte int32 arrays, 2-byte LRU order) and
+    refuses before touching CUDA (no device here)."""
+    def state(**kw):
+        f = dict(n_requests=2, n_positions=100, record_bytes=64, slots=8, host_records=4096,
+                 cache=8192, page_table=12288, slot_pos=16384, stamps=20480, lru=24576,
+                 resolves=28672)
+        f.update(kw)
+        return _native.LayerState(**f)
+
+    call = lib.hs_resolve_noalloc
+    for bad in (dict(host_records=4104), dict(cache=8200), dict(page_table=12290),
+                dict(slot_pos=16385), dict(stamps=20482), dict(lru=24577), dict(resolves=28673)):
+        assert call(ctypes.byref(state(**bad)), 1, None, 32768, 4, 36864, None, None) == \
+            hs.HS_ERR_INVALID_ARG, bad
+    s = state()
+    assert call(ctypes.byref(s), 1, None, 32770, 4, 36864, None, None) == hs.HS_ERR_INVALID_ARG
+    assert call(ctypes.byref(s), 1, None, 32768, 4, 36866, None, None) == hs.HS_ERR_INVALID_ARG
+    assert call(ctypes.byref(s), 1, 40962, 32768, 4, 36864, None, None) == hs.HS_ERR_INVALID_ARG
+    assert call(ctypes.byref(s), 1, None, 32768, 4, 36864, 45058, None) == hs.HS_ERR_INVALID_ARG

@@ -6,7 +6,7 @@ import torch
 from hierarchical_kv_cache_resolve_gb300 import hs
 from oracle.oracle import OK, Pair
 from tests.gpu_harness import check_cache, check_metadata, fill_selected
-from workloads import configs, records
+from workloads import configs, records, traces
 
 pytestmark = pytest.mark.gpu
 
@@ -298,6 +298,57 @@ def test_corrupted_plans_stay_exact():
         assert st["plan_mismatches"] > 0 and st["status"] & hs.HS_STATUS_PLAN
 
 
+def test_anchor_plan_replayed_into_a_diverged_layer_stays_exact():
+    """The anchor's miss plan replayed into two layers that share its
+    selection, one of which is given its own selection at a few steps, so
+    its history (and from then on its misses and victims) differs from the
+    anchor's: the copy writes slots that layer does not want, the consuming
+    resolve re-fetches what does not match and refills what the copy
+    overwrote, and every output, slot map, page table and slot content is
+    the oracle's.  The layer that keeps the anchor's history matches every
+    plan pair."""
+    w = _small(n_layers=3, layer_anchor=(0, 0, 0), steps=16, k=48, slots=64)
+    sel = _random_trace(w, seed=23)
+    own = sel[:, :, 2].copy()
+    sel[:, :, 1] = sel[:, :, 0]
+    sel[:, :, 2] = sel[:, :, 0]
+    for t in (5, 6, 11):
+        sel[t, :, 2] = own[t]
+    R, k = w.n_requests, w.k
+    orc = _oracles(w)
+    with hs.Pool.for_workload(w) as pool:
+        fill_selected(pool, w, sel)
+        out = torch.empty((3, R, k), dtype=torch.int32, device="cuda")
+        plan = torch.empty(hs.hs_plan_bytes(R, k), dtype=torch.uint8, device="cuda")
+        side = torch.cuda.Stream()
+        main = torch.cuda.current_stream()
+        for t in range(w.steps):
+            s = [torch.from_numpy(np.ascontiguousarray(sel[t, :, l])).cuda() for l in range(3)]
+            pool.resolve_anchor(0, s[0], out[0], plan)
+            for l in (1, 2):
+                ev = torch.cuda.Event()
+                ev.record(main)
+                side.wait_event(ev)
+                pool.prefetch_copy(l, R, k, plan, stream=side)
+                ev2 = torch.cuda.Event()
+                ev2.record(side)
+                main.wait_event(ev2)
+                pool.resolve(l, s[l], out[l], plan=plan)
+            got = out.cpu().numpy()
+            for l in range(3):
+                for r in range(R):
+                    want = orc[(r, l)].resolve(sel[t, r, l], out_base=r * w.slots)[1]
+                    assert np.array_equal(got[l, r], want), (t, l, r)
+        for (r, l), p in orc.items():
+            check_metadata(pool, w, l, r, p, w.steps)
+            check_cache(pool, w, l, r, p.slot_pos)
+        s1, s2 = pool.stats(1), pool.stats(2)
+        assert s1["status"] == 0 and s2["status"] == 0
+        assert s1["plan_mismatches"] == 0 and s1["plan_hits"] == s1["misses"]
+        assert s1["fetched_bytes"] == 0
+        assert s2["plan_mismatches"] > 0 and s2["fetched_bytes"] > 0
+
+
 def test_cuda_graph_replay_matches_oracle():
     w = configs.DSA_MLA.with_(n_requests=4, n_positions=20000, steps=20)
     from workloads import traces
@@ -352,9 +403,37 @@ def test_pools_of_different_sizes_coexist():
                 assert np.array_equal(gs[r], orc_s[(r, 0)].resolve(sel_s[t, r, 0], out_base=r * small.slots)[1])
 
 
-def test_link_probe_reports_bandwidth():
-    h2d, gather = hs.hs_link_probe(256 << 20, reps=3, record_bytes=1152)
+@pytest.mark.parametrize("kind", [hs.HS_HOST_ALLOC_PINNED, hs.HS_HOST_ALLOC_VMM_NUMA])
+def test_link_probe_reports_bandwidth(kind):
+    h2d, gather = hs.hs_link_probe(256 << 20, reps=3, record_bytes=1152, host_alloc=kind)
     assert h2d > 1.0 and gather > 1.0
+
+
+@pytest.mark.parametrize("kind", [hs.HS_HOST_ALLOC_PINNED, hs.HS_HOST_ALLOC_VMM_NUMA])
+def test_pool_with_each_host_allocation(kind):
+    """Both host allocations hold the records the kernels fetch: the same
+    trace gives the oracle's slots and slot contents either way."""
+    w = configs.TINY.with_(n_requests=3, n_layers=2, steps=12)
+    sel = traces.generate(w)
+    orc = _oracles(w)
+    with hs.Pool.for_workload(w, host_alloc=kind) as pool:
+        info = pool.info()
+        assert info["host_alloc"] == kind
+        assert info["host_bytes"] == w.host_bytes and info["host_mapped_bytes"] >= w.host_bytes
+        if kind == hs.HS_HOST_ALLOC_VMM_NUMA and info["device_numa"] >= 0 \
+                and info["host_numa_first"] >= 0:
+            assert info["host_numa_first"] == info["device_numa"]
+        fill_selected(pool, w, sel)
+        out = torch.empty((w.n_requests, w.k), dtype=torch.int32, device="cuda")
+        for t in range(w.steps):
+            for l in range(w.n_layers):
+                pool.resolve(l, torch.from_numpy(np.ascontiguousarray(sel[t, :, l])).cuda(), out)
+                got = out.cpu().numpy()
+                for r in range(w.n_requests):
+                    want = orc[(r, l)].resolve(sel[t, r, l], out_base=r * w.slots)[1]
+                    assert np.array_equal(got[r], want), (t, r, l)
+        for (r, l), p in orc.items():
+            check_cache(pool, w, l, r, p.slot_pos)
 
 
 def test_host_records_layout():

@@ -47,25 +47,33 @@ def run_and_compare(w, meta_every=1, cache_sample=None, prefetch=False, sel=None
         main = torch.cuda.current_stream()
         side = torch.cuda.Stream()
         plans = {}
+        replay = prefetch == "replay"
         if prefetch:
             nb = hs.hs_plan_bytes(R, k)
             for l in range(NL):
-                if w.anchors[l] != l:
+                # "plan": one plan per shared layer (hs_prefetch_plan);
+                # "replay": one per anchor, written by its resolve
+                if (w.anchors[l] != l) != replay:
                     plans[l] = torch.empty(nb, dtype=torch.uint8, device="cuda")
+        shared = {l for l in range(NL) if w.anchors[l] != l} if prefetch else set()
         prev = {l: 0 for l in range(NL)}
         for t in range(T):
             for l in range(NL):
                 a = w.anchors[l]
-                if l in plans:
-                    pool.prefetch_plan(a, l, dsel[t, l], plans[l], stream=main)
+                if l in shared:
+                    plan = plans[a] if replay else plans[l]
+                    if not replay:
+                        pool.prefetch_plan(a, l, dsel[t, l], plan, stream=main)
                     ev = torch.cuda.Event()
                     ev.record(main)
                     side.wait_event(ev)
-                    pool.prefetch_copy(l, R, k, plans[l], stream=side)
+                    pool.prefetch_copy(l, R, k, plan, stream=side)
                     ev2 = torch.cuda.Event()
                     ev2.record(side)
                     main.wait_event(ev2)
-                    pool.resolve(l, dsel[t, l], out[l], plan=plans[l], stream=main)
+                    pool.resolve(l, dsel[t, l], out[l], plan=plan, stream=main)
+                elif replay and l in plans:
+                    pool.resolve_anchor(l, dsel[t, l], out[l], plans[l], stream=main)
                 else:
                     pool.resolve(l, dsel[t, l], out[l], stream=main)
             ores = _oracle_step(orc, sel[t], ex)
@@ -89,7 +97,7 @@ def run_and_compare(w, meta_every=1, cache_sample=None, prefetch=False, sel=None
             assert st["hits"] == sum(p.hits for p in ps)
             assert st["misses"] == sum(p.misses for p in ps)
             assert st["status"] == 0
-            if l in plans:
+            if l in shared:
                 assert st["plan_mismatches"] == 0
                 assert st["plan_hits"] == st["misses"]
                 assert st["prefetched_bytes"] == st["misses"] * w.record_bytes
@@ -136,11 +144,20 @@ def test_tight_prefetch_full_with_prefetch():
     run_and_compare(configs.TIGHT_PREFETCH, meta_every=32, cache_sample=256, prefetch=True)
 
 
+@pytest.mark.slow
+def test_tight_prefetch_full_with_anchor_replay():
+    """The anchor's resolve writes its miss plan; the copy-only kernel
+    replays it into the three layers sharing the anchor's selection, whose
+    resolves consume it: every plan pair matches, nothing is fetched twice."""
+    run_and_compare(configs.TIGHT_PREFETCH, meta_every=32, cache_sample=256, prefetch="replay")
+
+
 def test_tight_prefetch_small_with_and_without_prefetch():
     w = configs.TIGHT_PREFETCH.with_(n_requests=6, n_positions=20000, k=512, slots=512,
                                      steps=24)
     run_and_compare(w, meta_every=4, prefetch=False)
     run_and_compare(w, meta_every=4, prefetch=True)
+    run_and_compare(w, meta_every=4, prefetch="replay")
 
 
 @pytest.mark.slow
@@ -186,7 +203,8 @@ def test_dsa_mla_full_as_the_benchmark_runs_it():
     ex.shutdown()
 
 
-def test_tight_prefetch_scheduled_like_the_overlap_benchmark():
+@pytest.mark.parametrize("source", ["plan", "replay"])
+def test_tight_prefetch_scheduled_like_the_overlap_benchmark(source):
     """Exact prefetch in the schedule of the overlap benchmark: at each
     anchor the plans and copies of the layers sharing its selection run on a
     side stream, concurrently with the anchor's resolve and with the
@@ -214,8 +232,10 @@ def test_tight_prefetch_scheduled_like_the_overlap_benchmark():
         dsel = device_trace(sel)
         out = torch.empty((T, NL, R, k), dtype=torch.int32, device="cuda")
         att = torch.empty((T, NL, R, heads, 512), dtype=torch.float32, device="cuda")
+        replay = source == "replay"
+        shared = [l for l in range(NL) if w.anchors[l] != l]
         plans = {l: torch.empty(hs.hs_plan_bytes(R, k), dtype=torch.uint8, device="cuda")
-                 for l in range(NL) if w.anchors[l] != l}
+                 for l in range(NL) if (w.anchors[l] != l) != replay}
         caches = [pool.views(l)["cache"] for l in range(NL)]
         main, side = torch.cuda.current_stream(), torch.cuda.Stream()
         torch.cuda.synchronize()
@@ -223,18 +243,25 @@ def test_tight_prefetch_scheduled_like_the_overlap_benchmark():
             evs = {}
             for l in range(NL):
                 if w.anchors[l] == l:
+                    if replay:
+                        # the anchor's resolve writes the plan; the copies
+                        # replay it from there on, beside the compute
+                        pool.resolve_anchor(l, dsel[t, l], out[t, l], plans[l], stream=main)
                     ready = torch.cuda.Event()
                     ready.record(main)
                     side.wait_event(ready)
-                    for l2 in plans:
+                    for l2 in shared:
                         if w.anchors[l2] == l:
-                            pool.prefetch_plan(l, l2, dsel[t, l2], plans[l2], stream=side)
-                            pool.prefetch_copy(l2, R, k, plans[l2], stream=side)
+                            if not replay:
+                                pool.prefetch_plan(l, l2, dsel[t, l2], plans[l2], stream=side)
+                            pool.prefetch_copy(l2, R, k, plans[l if replay else l2], stream=side)
                             evs[l2] = torch.cuda.Event()
                             evs[l2].record(side)
-                    pool.resolve(l, dsel[t, l], out[t, l], stream=main)
+                    if not replay:
+                        pool.resolve(l, dsel[t, l], out[t, l], stream=main)
                 else:
-                    pool.resolve(l, dsel[t, l], out[t, l], plan=plans[l], stream=main)
+                    pool.resolve(l, dsel[t, l], out[t, l],
+                                 plan=plans[w.anchors[l] if replay else l], stream=main)
                 hs.hs_sparse_attention(q, caches[l], R * w.slots, out[t, l], R, k, heads,
                                        scale, att[t, l], stream=main)
                 if l + 1 in evs:
@@ -253,7 +280,7 @@ def test_tight_prefetch_scheduled_like_the_overlap_benchmark():
         for l in range(NL):
             st = pool.stats(l)
             assert st["status"] == 0 and st["resolves"] == T * R
-            if l in plans:
+            if l in shared:
                 assert st["plan_mismatches"] == 0 and st["fetched_bytes"] == 0
                 assert st["prefetched_bytes"] == st["misses"] * w.record_bytes
         # what each layer's attention read was the selection's records

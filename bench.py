@@ -52,6 +52,7 @@ if ROOT not in sys.path:
 METRIC = ("resolves/sec and miss-fetch GB/s (fraction of measured pinned H2D BW) "
           "at 1 GB300")
 L2_FLUSH_BYTES = 256 << 20
+HOST_ALLOC = {"auto": 0, "pinned": 1, "vmm": 2}
 CONT_STEPS, CONT_BLOCKS = 16, 3
 
 # Counters of one steady-state resolve launch from an ncu capture (dsa_mla
@@ -116,6 +117,55 @@ def hbm_sector_bytes_per_resolve(k: int, B: int, m: float, W: int) -> float:
     reads = 4 * k + 4 * B + 2 * B + 32 * k
     writes = 4 * k + 32 * stamp_sectors + 32 * m + 64 * m + 2 * B + m * W
     return reads + writes
+
+
+def host_pages(addr: int, nbytes: int) -> dict:
+    """How the host pool's pages are backed, from /proc/self/smaps: the
+    mappings overlapping [addr, addr + nbytes) summed (kB), their page
+    sizes, and the system's transparent-huge-page settings.  The GPU's
+    scattered reads of pinned host memory depend on the pages behind it."""
+    res = {"mappings": 0, "size_kb": 0, "rss_kb": 0, "anon_huge_kb": 0,
+           "kernel_page_kb": set(), "mmu_page_kb": set()}
+    lo, hi = addr, addr + nbytes
+    try:
+        with open("/proc/self/smaps") as f:
+            cur = False
+            for line in f:
+                head = line.split()
+                if not head:
+                    continue
+                if "-" in head[0] and len(head) >= 5 and ":" not in head[0]:
+                    a, b = (int(x, 16) for x in head[0].split("-"))
+                    cur = a < hi and b > lo
+                    if cur:
+                        res["mappings"] += 1
+                    continue
+                if not cur:
+                    continue
+                key = head[0].rstrip(":")
+                if key == "Size":
+                    res["size_kb"] += int(head[1])
+                elif key == "Rss":
+                    res["rss_kb"] += int(head[1])
+                elif key == "AnonHugePages":
+                    res["anon_huge_kb"] += int(head[1])
+                elif key == "KernelPageSize":
+                    res["kernel_page_kb"].add(int(head[1]))
+                elif key == "MMUPageSize":
+                    res["mmu_page_kb"].add(int(head[1]))
+    except OSError as e:
+        res["error"] = str(e)
+    res["kernel_page_kb"] = sorted(res["kernel_page_kb"])
+    res["mmu_page_kb"] = sorted(res["mmu_page_kb"])
+    thp = {}
+    for name in ("enabled", "defrag", "hpage_pmd_size"):
+        try:
+            with open(f"/sys/kernel/mm/transparent_hugepage/{name}") as f:
+                thp[name] = f.read().strip()
+        except OSError:
+            pass
+    res["thp"] = thp
+    return res
 
 
 def load_peaks():
@@ -281,29 +331,37 @@ def cpu_model() -> str:
     return platform.machine()
 
 
+CPU_SAMPLE_PAIRS = 32
+
+
 def cpu_baseline(w, threads: int, epochs: int = 4):
-    """The oracle over the whole trace of every pair, replayed `epochs` times
-    back to back (steps past the end wrap around, as in the GPU passes):
-    about ten seconds of CPU work for the dsa_mla workload."""
-    pairs = w.n_requests * w.n_layers
+    """The oracle on a bounded sample of the workload: the first
+    CPU_SAMPLE_PAIRS (request, layer) pairs (all of them for the smaller
+    workloads), each replayed over its whole trace `epochs` times back to
+    back (steps past the end wrap around, as in the GPU passes), one thread
+    per pair; and one pair on one thread.  About ten seconds of CPU work."""
+    pairs = min(w.n_requests * w.n_layers, CPU_SAMPLE_PAIRS)
     steps = epochs * w.steps
     value, wall, n, fetched = time_oracle(w, pairs, steps, threads)
     one, one_wall, one_n, _ = time_oracle(w, 1, steps, 1)
-    return {"value": value, "unit": "resolves/s", "cores": threads, "kind": "oracle",
+    return {"value": value, "unit": "resolves/s", "cores": min(threads, pairs), "kind": "oracle",
             "cpu_model": cpu_model(),
             "single_thread": {"value": one, "unit": "resolves/s",
                               "sample": f"one (request, layer) pair x {steps} steps, one thread",
                               "wall_s": one_wall},
-            "sample": (f"all {pairs} (request, layer) pairs x {steps} steps ({epochs} passes "
-                       f"over the {w.name} trace; {n} resolves, {fetched / 1e9:.2f} GB of "
-                       f"misses copied), one thread per pair, {threads} threads"),
+            "sample": (f"{pairs} of the {w.n_requests * w.n_layers} (request, layer) pairs x "
+                       f"{steps} steps ({epochs} passes over the {w.name} trace; {n} resolves, "
+                       f"{fetched / 1e9:.2f} GB of misses copied), one thread per pair, "
+                       f"{min(threads, pairs)} threads"),
             "wall_s": wall, "cpu_s": wall * min(threads, pairs),
             "miss_fetch_gbs": fetched / wall / 1e9}
 
 
 # -------------------------------------------------------------- GPU arm ----
 
-def run_gpu(args, w, rank, world, dist_on):
+def run_gpu(args, w, rank, world, dist_on, lite=False):
+    """All GPU passes on workload `w`; `lite`: the graph pass (`value`) and
+    its roofline only (a second workload reported beside the headline)."""
     import torch
 
     from hierarchical_kv_cache_resolve_gb300 import hs
@@ -314,14 +372,19 @@ def run_gpu(args, w, rank, world, dist_on):
     pci = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
     R, NL, k, B, W, T = w.n_requests, w.n_layers, w.k, w.slots, w.record_bytes, w.steps
 
-    h2d_gbs, gather_gbs = hs.hs_link_probe(1 << 30, 10, W)
+    kind = HOST_ALLOC[args.host_alloc]
+    h2d_gbs, gather_gbs = hs.hs_link_probe(1 << 30, 10, W, kind)
 
     sel = traces.generate(w)
     dsel = torch.from_numpy(np.ascontiguousarray(sel.transpose(0, 2, 1, 3))).to(dev)
-    pool = hs.Pool.for_workload(w)
+    t_fill = time.perf_counter()
+    pool = hs.Pool.for_workload(w, host_alloc=kind)
+    pool_info = pool.info()
     for r in range(R):
         for l in range(NL):
             records.fill(pool.host_records(r, l).ctypes.data, w, r, l)
+    pool_info["create_and_fill_s"] = time.perf_counter() - t_fill
+    pool_info["pages"] = host_pages(pool.host_records(0, 0).ctypes.data, w.host_bytes)
     out = torch.empty((NL, R, k), dtype=torch.int32, device=dev)
     flush = L2Flush(dev)
     main = torch.cuda.current_stream()
@@ -397,6 +460,29 @@ def run_gpu(args, w, rank, world, dist_on):
     hbm_per_launch = R * hbm_bytes_per_resolve(k, B, m_per_resolve, W)
     hbm_sectors_per_launch = R * hbm_sector_bytes_per_resolve(k, B, m_per_resolve, W)
 
+    if lite:
+        pool.close()
+        return {
+            "workload": workload_name(w), "resolves_per_s": total_resolves / dev_s_max,
+            "ms_per_step": dev_s_max / K * 1e3, "steps": K, "warmup": Wm,
+            "miss_rate": misses / (resolves * k),
+            "miss_fetch_gbs": total_fetched / dev_s_max / 1e9,
+            "roofline": {"kernel": "resolve_kernel", "bound": "link",
+                         "achieved": link_bytes_per_launch / avg_launch_s / 1e9,
+                         "peak": h2d_gbs, "unit": "GB/s",
+                         "frac": link_bytes_per_launch / avg_launch_s / 1e9 / h2d_gbs,
+                         "algorithmic_bytes_per_launch": link_bytes_per_launch,
+                         "avg_launch_us": avg_launch_s * 1e6},
+            "repeats": [len(g) * R * NL / (sum(g) / 1e3)
+                        for g in np.array_split(np.array(step_ms), 3) if len(g)],
+            "cold_step_ms": cold_ms, "host_pool": pool_info,
+            "l2": "flushed before every timed step"}
+
+    # ---- exact prefetch in the pure resolve step, and the copy-only rate of
+    # the same miss records (both beside `value`) ----------------------------
+    prefetch_on = run_prefetch_pass(pool, w, dsel, flush, main, cap, K, Wm, h2d_gbs)
+    copy_only = run_copy_only(pool, w, dsel, flush, main, cap, K, Wm, h2d_gbs)
+
     # ---- continuous pass (diagnostic, not `value`) --------------------------
     # blocks of CONT_STEPS consecutive steps captured as one graph, L2
     # flushed before each block only: the per-launch time of decode steps
@@ -436,6 +522,9 @@ def run_gpu(args, w, rank, world, dist_on):
         "miss_fetch_gbs": cont_bytes / cont_s / 1e9,
         "frac_of_h2d": cont_bytes / cont_s / 1e9 / h2d_gbs,
     }
+
+    # ---- measurement passes: no fetch, stage stamps (diagnostics) ------------
+    measure = run_measure_passes(pool, w, dsel, flush, main, cap, K, Wm)
 
     # ---- kernel pass (per-launch events, eager launches) ---------------------
     pool.reset()
@@ -548,6 +637,7 @@ def run_gpu(args, w, rank, world, dist_on):
             "avg_launch_us": avg_launch_s * 1e6,
             "avg_launch_from": "graph-timed steps / launches per step",
             "avg_launch_us_eager": avg_launch_eager_s * 1e6,
+            "frac_of_copy_only": link_achieved / copy_only["link_gbs"] if copy_only else None,
         },
         "roofline_hbm": {
             "kernel": "resolve_kernel",
@@ -570,7 +660,11 @@ def run_gpu(args, w, rank, world, dist_on):
                     "hs_resolve per layer, D2H of the published slots) and a stream "
                     "synchronize; wall clock",
         },
+        "prefetch_on": prefetch_on,
+        "copy_only": copy_only,
         "continuous": continuous,
+        "no_fetch": measure["no_fetch"],
+        "stages": measure["stages"],
         "repeats": {
             "what": "the timed steps in three consecutive groups, each as resolves/s "
                     "(rank 0's device time)",
@@ -586,9 +680,291 @@ def run_gpu(args, w, rank, world, dist_on):
             "miss_fetch_gbs": st_cold["fetched_bytes"] / (cold_ms / 1e3) / 1e9,
         },
         "gpu_launches": K * launches_per_step,
+        "host_pool": pool_info,
         "clocks": sampler.summary(),
         "graph_wall_s": wall_graph,
     }
+    return res
+
+
+def _timed_graph_steps(graphs, flush, main):
+    """Replays the per-step graphs, L2 flushed before each, events on the
+    launching stream around each replay; returns the steps' milliseconds."""
+    import torch
+    ms = []
+    for i, g in enumerate(graphs):
+        flush(i)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(main)
+        g.replay()
+        e1.record(main)
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    return ms
+
+
+def run_prefetch_pass(pool, w, dsel, flush, main, cap, K, Wm, h2d_gbs):
+    """The timed steps with exact layer-wise prefetch by anchor-plan replay.
+
+    Per step, in layer order: an anchor's resolve (hs_resolve_anchor) writes
+    its miss plan; a side stream, forked after it, replays the plan into
+    each layer sharing the anchor's selection (hs_prefetch_copy); each such
+    layer's resolve waits for its copy and consumes the plan (it commits
+    the metadata and fetches only what does not match).  One graph per
+    step, L2 flushed before every step.  Without compute between the
+    layers the copies can only overlap other resolves, so this measures
+    what the replay costs or saves in a pure resolve step."""
+    import torch
+
+    from hierarchical_kv_cache_resolve_gb300 import hs
+    R, NL, k, T = w.n_requests, w.n_layers, w.k, w.steps
+    shared = [l for l in range(NL) if w.anchors[l] != l]
+    if not shared:
+        return None
+    anchors = sorted({w.anchors[l] for l in shared})
+    plans = {a: torch.empty(hs.hs_plan_bytes(R, k), dtype=torch.uint8, device=dsel.device)
+             for a in anchors}
+    out = torch.empty((NL, R, k), dtype=torch.int32, device=dsel.device)
+    side = torch.cuda.Stream()
+
+    def step(t, stream):
+        evs = {}
+        for l in range(NL):
+            if l in plans:
+                pool.resolve_anchor(l, dsel[t, l], out[l], plans[l], stream=stream)
+                fork = torch.cuda.Event()
+                fork.record(stream)
+                side.wait_event(fork)
+                for l2 in shared:
+                    if w.anchors[l2] == l:
+                        pool.prefetch_copy(l2, R, k, plans[l], stream=side)
+                        evs[l2] = torch.cuda.Event()
+                        evs[l2].record(side)
+            elif l in evs:
+                stream.wait_event(evs[l])
+                pool.resolve(l, dsel[t, l], out[l], plan=plans[w.anchors[l]], stream=stream)
+            else:
+                pool.resolve(l, dsel[t, l], out[l], stream=stream)
+
+    pool.reset()
+    for s in range(Wm):
+        step(s % T, main)
+    torch.cuda.synchronize()
+    graphs = []
+    for i in range(K):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            step((Wm + i) % T, cap)
+        graphs.append(g)
+    st0 = pool.stats(check=False)
+    ms = _timed_graph_steps(graphs, flush, main)
+    st1 = pool.stats(check=False)
+    del graphs
+    d = {x: st1[x] - st0[x] for x in ("resolves", "misses", "fetched_bytes", "prefetched_bytes",
+                                      "plan_hits", "plan_mismatches")}
+    sec = sum(ms) / 1e3
+    link = (d["fetched_bytes"] + d["prefetched_bytes"]) / sec / 1e9
+    pool.reset()
+    return {"what": "exact prefetch by anchor-plan replay in the pure resolve step "
+                    "(hs_resolve_anchor, hs_prefetch_copy on a side stream, plan-consuming "
+                    "hs_resolve); per-step graphs, L2 flushed before every step",
+            "resolves_per_s": d["resolves"] / sec, "ms_per_step": sum(ms) / K,
+            "counters": d, "status": st1["status"],
+            "link_gbs": link, "frac_of_h2d": link / h2d_gbs,
+            "kernels_per_step": NL + len(shared),
+            "repeats": [len(g) * R * NL / (sum(g) / 1e3)
+                        for g in np.array_split(np.array(ms), 3) if len(g)]}
+
+
+def run_copy_only(pool, w, dsel, flush, main, cap, K, Wm, h2d_gbs):
+    """The copy-only rate of exactly the records the timed steps miss.
+
+    The timed steps are resolved once with every layer writing its miss
+    plan (hs_resolve_anchor); then, after a reset, the copy-only kernel
+    (hs_prefetch_copy, a full-GPU grid of 16-byte loads and nothing else)
+    moves each step's planned records into their slots, one graph per step
+    and the L2 flushed before each.  The resolve's own link rate divided by
+    this one says how close the fused kernel comes to moving the same host
+    records with no decision, metadata or staging around the loads; on a
+    pool past the GPU's host translation reach both are bound by it."""
+    import torch
+
+    from hierarchical_kv_cache_resolve_gb300 import hs
+    R, NL, k, T = w.n_requests, w.n_layers, w.k, w.steps
+    nb = hs.hs_plan_bytes(R, k)
+    plans = torch.empty((K, NL, nb), dtype=torch.uint8, device=dsel.device)
+    out = torch.empty((NL, R, k), dtype=torch.int32, device=dsel.device)
+    pool.reset()
+    for s in range(Wm):
+        for l in range(NL):
+            pool.resolve(l, dsel[s % T, l], out[l], stream=main)
+    for i in range(K):
+        for l in range(NL):
+            pool.resolve_anchor(l, dsel[(Wm + i) % T, l], out[l], plans[i, l], stream=main)
+    torch.cuda.synchronize()
+    graphs = []
+    for i in range(K):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            for l in range(NL):
+                pool.prefetch_copy(l, R, k, plans[i, l], stream=cap)
+        graphs.append(g)
+    st0 = pool.stats(check=False)
+    ms = _timed_graph_steps(graphs, flush, main)
+    st1 = pool.stats(check=False)
+    del graphs
+    moved = st1["prefetched_bytes"] - st0["prefetched_bytes"]
+    sec = sum(ms) / 1e3
+    pool.reset()
+    return {"what": "the timed steps' miss records moved by hs_prefetch_copy alone (plans "
+                    "written by the resolves), per-step graphs of one copy per layer, L2 "
+                    "flushed before every step",
+            "bytes": moved, "link_gbs": moved / sec / 1e9,
+            "frac_of_h2d": moved / sec / 1e9 / h2d_gbs, "ms_per_step": sum(ms) / K,
+            "status": st1["status"]}
+
+
+def metadata_bytes_per_resolve(k: int, B: int, m: float) -> float:
+    """Algorithmic HBM bytes of one resolve without its records (the no-fetch
+    variant): hbm_bytes_per_resolve less the m * W record bytes."""
+    return hbm_bytes_per_resolve(k, B, m, 0)
+
+
+STAGE_US = (
+    # (name, what, later stamp, earlier stamp, CTA: leader / followers)
+    ("leader_load", "selection, slot map, LRU order into shared memory", "LOADED", "ENTRY", "L"),
+    ("leader_hash", "validate + hash build + membership bits", "HASHED", "LOADED", "L"),
+    ("leader_probe", "probe every slot (mark hits)", "PROBED", "HASHED", "L"),
+    ("leader_victims", "rank misses, choose LRU victims", "DECIDED", "PROBED", "L"),
+    ("leader_wait_check", "previous grid complete, decision checked", "CHECKED", "DECIDED", "L"),
+    ("leader_to_verdict", "cluster barrier publishing the decision", "VERDICT", "CHECKED", "L"),
+    ("leader_commit", "page table, slot map, stamps, LRU order, counter", "COMMITTED", "VERDICT",
+     "L"),
+)
+
+
+def summarise_stamps(a, C):
+    """Stage durations of resolve launches from hs_resolve_measure stamps.
+
+    `a` is [launches][R][8][16] u64 (ns).  Per launch, t0 = the earliest CTA
+    entry; per request the leader's phases (STAGE_US) and the followers'
+    fetch milestones relative to t0 (first staging copy issued, staged
+    records landed, slot stores issued), then medians over requests and
+    launches (microseconds).  `fetch` = last landing - first issue per
+    request: the host-link transfer; `decision` = leader entry to decision."""
+    from hierarchical_kv_cache_resolve_gb300 import hs
+    S = hs.HS_STAMP
+    a = a.astype(np.float64)
+    rows = []
+    for launch in a:
+        t0 = launch[:, :C, S["ENTRY"]].min()
+        span = launch[:, :C, S["EXIT"]].max() - t0
+        for req in launch:
+            ld = req[0]
+            d = {name: (ld[S[hi]] - ld[S[lo]]) / 1e3 for name, _, hi, lo, _ in STAGE_US}
+            d["leader_start"] = (ld[S["ENTRY"]] - t0) / 1e3
+            d["decision_done"] = (ld[S["DECIDED"]] - t0) / 1e3
+            d["commit_done"] = (ld[S["COMMITTED"]] - t0) / 1e3
+            d["launch_span"] = span / 1e3
+            d["attempts"] = ld[S["ATTEMPTS"]]
+            if C > 1:
+                f = req[1:C]
+                d["first_host_load_issued"] = (f[:, S["F_ISSUE"]][f[:, S["F_ISSUE"]] > 0].min()
+                                               - t0) / 1e3 if (f[:, S["F_ISSUE"]] > 0).any() else None
+                d["staging_issued"] = (f[:, S["F_ISSUED"]].max() - t0) / 1e3
+                d["staged_landed"] = (f[:, S["F_LANDED"]].max() - t0) / 1e3
+                d["slots_stored"] = (f[:, S["F_STORED"]].max() - t0) / 1e3
+            rows.append(d)
+    out = {}
+    for key in rows[0]:
+        vals = [r[key] for r in rows if r.get(key) is not None]
+        out[key] = float(np.median(vals)) if vals else None
+    if out.get("staged_landed") is not None and out.get("first_host_load_issued") is not None:
+        out["fetch"] = out["staged_landed"] - out["first_host_load_issued"]
+    return out
+
+
+def run_measure_passes(pool, w, dsel, flush, main, cap, K, Wm):
+    """Two diagnostics beside `value` (same steps, per-step graphs, L2
+    flushed before every step, pool reset first):
+
+    no_fetch -- hs_resolve_measure(HS_MEASURE_NO_FETCH): the resolve with
+       every metadata step and no host fetch; per-launch time and the
+       metadata HBM roofline (the no-IO analogue of the pages' no-IO run);
+    stages   -- the resolve with stage timestamps (%globaltimer): a
+       miss-resolution breakdown per launch (summarise_stamps).
+    """
+    import torch
+
+    from hierarchical_kv_cache_resolve_gb300 import hs
+    R, NL, k, B, T = w.n_requests, w.n_layers, w.k, w.slots, w.steps
+    out = torch.empty((NL, R, k), dtype=torch.int32, device=dsel.device)
+    slots = hs.hs_measure_stamp_slots()
+    res = {}
+    for name, flags, stamped in (("no_fetch", hs.HS_MEASURE_NO_FETCH, False),
+                                 ("stages", 0, True)):
+        pool.reset()
+        times = (torch.zeros((K, NL, R, slots), dtype=torch.int64, device=dsel.device)
+                 if stamped else None)
+        for s in range(Wm):
+            for l in range(NL):
+                pool.resolve_measure(l, dsel[s % T, l], out[l], flags=flags, stream=main)
+        graphs = []
+        for i in range(K):
+            g = torch.cuda.CUDAGraph()
+            t = (Wm + i) % T
+            with torch.cuda.graph(g, stream=cap):
+                for l in range(NL):
+                    pool.resolve_measure(l, dsel[t, l], out[l], flags=flags,
+                                         times=times[i, l] if stamped else None, stream=cap)
+            graphs.append(g)
+        st0 = pool.stats(check=False)
+        ms = 0.0
+        for i in range(K):
+            flush(i)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(main)
+            graphs[i].replay()
+            e1.record(main)
+            torch.cuda.synchronize()
+            ms += e0.elapsed_time(e1)
+        st1 = pool.stats(check=False)
+        del graphs
+        launches = K * NL
+        us = ms * 1e3 / launches
+        m = (st1["misses"] - st0["misses"]) / max(1, st1["resolves"] - st0["resolves"])
+        entry = {"what": ("hs_resolve_measure without the fetch, per-step graphs, L2 flushed "
+                          "before every step" if not stamped else
+                          "hs_resolve_measure with %globaltimer stage stamps, per-step graphs, "
+                          "L2 flushed before every step; medians over requests and launches, "
+                          "microseconds from the launch's first CTA entry"),
+                 "us_per_launch": us, "resolves_per_s": launches * R / (ms / 1e3),
+                 "misses_per_resolve": m, "status": st1["status"]}
+        if not stamped:
+            peaks = load_peaks()
+            hbm = peaks.get("hbm_gbs") if peaks else None
+            meta = R * metadata_bytes_per_resolve(k, B, m)
+            achieved = meta / (us * 1e-6) / 1e9
+            entry["roofline_hbm_metadata"] = {
+                "kernel": "resolve_kernel (no fetch)", "bound": "hbm", "achieved": achieved,
+                "peak": hbm, "unit": "GB/s", "frac": achieved / hbm if hbm else None,
+                "algorithmic_bytes_per_launch": meta,
+                "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if hbm else None}
+        else:
+            a = times.cpu().numpy().reshape(K, NL, R, 8, 16)
+            C = 1
+            while C < 8 and a[:, :, :, C, hs.HS_STAMP["ENTRY"]].any():
+                C += 1
+            entry["cluster_ctas"] = C
+            entry["median_us"] = summarise_stamps(a.reshape(K * NL, R, 8, 16), C)
+            # the first launch of a step has no launch ahead of it to overlap
+            entry["first_launch_of_step_median_us"] = summarise_stamps(a[:, 0], C)
+            if NL > 1:
+                entry["later_launches_median_us"] = summarise_stamps(
+                    a[:, 1:].reshape(K * (NL - 1), R, 8, 16), C)
+            entry["stage_legend"] = {name: what for name, what, _, _, _ in STAGE_US}
+        res[name] = entry
+    pool.reset()
     return res
 
 
@@ -630,8 +1006,12 @@ def run_prefetch_overlap(args, w):
     B = w.slots
     out = (torch.arange(R, dtype=torch.int32, device=dev)[:, None] * B
            + torch.arange(k, dtype=torch.int32, device=dev)[None, :]).repeat(NL, 1, 1)
+    replay = args.prefetch_source == "replay"
+    shared = [l for l in range(NL) if w.anchors[l] != l]
+    # replay: one plan per anchor, written by its resolve; plan: one per
+    # shared layer, written by hs_prefetch_plan
     plans = {l: torch.empty(hs.hs_plan_bytes(R, k), dtype=torch.uint8, device=dev)
-             for l in range(NL) if w.anchors[l] != l}
+             for l in range(NL) if (w.anchors[l] != l) != replay}
     flush = L2Flush(dev)
     main, side = torch.cuda.current_stream(), torch.cuda.Stream()
 
@@ -672,24 +1052,31 @@ def run_prefetch_overlap(args, w):
             anc = w.anchors[l]
             if mode != "compute":
                 if l == anc:
+                    if mode == "on" and replay and l in plans:
+                        # the anchor's resolve writes its miss plan
+                        pool.resolve_anchor(l, dsel[t, l], out[l], plans[l], stream=main)
                     if mode == "on":
                         # The anchor's selection is known and the shared
                         # layers' previous resolves and attention calls are
-                        # behind this point of the main stream: plan and copy
-                        # their misses on the side stream from here on.
+                        # behind this point of the main stream (with replay,
+                        # the anchor's plan too): copy the shared layers'
+                        # misses on the side stream from here on.
                         ready = torch.cuda.Event()
                         ready.record(main)
                         side.wait_event(ready)
-                        for l2 in plans:
+                        for l2 in shared:
                             if w.anchors[l2] != l:
                                 continue
-                            pool.prefetch_plan(l, l2, dsel[t, l2], plans[l2], stream=side)
-                            pool.prefetch_copy(l2, R, k, plans[l2], stream=side)
+                            if not replay:
+                                pool.prefetch_plan(l, l2, dsel[t, l2], plans[l2], stream=side)
+                            pool.prefetch_copy(l2, R, k, plans[l if replay else l2], stream=side)
                             evs[l2] = torch.cuda.Event()
                             evs[l2].record(side)
-                    pool.resolve(l, dsel[t, l], out[l], stream=main)
+                    if not (mode == "on" and replay and l in plans):
+                        pool.resolve(l, dsel[t, l], out[l], stream=main)
                 elif mode == "on":
-                    pool.resolve(l, dsel[t, l], out[l], plan=plans[l], stream=main)
+                    pool.resolve(l, dsel[t, l], out[l], plan=plans[anc if replay else l],
+                                 stream=main)
                 else:
                     pool.resolve(l, dsel[t, l], out[l], stream=main)
             if mode != "resolve":
@@ -723,12 +1110,11 @@ def run_prefetch_overlap(args, w):
                                                           "plan_mismatches", "status")}
     attn_res = time_attention(lambda: attention(0), flush, main, R, k, heads,
                               args.steps) if attn else None
-    kern = time_prefetch_kernels(pool, w, dsel, out, plans, flush, main, args)
+    kern = time_prefetch_kernels(pool, w, dsel, out, plans, flush, main, args, replay)
     pool.close()
     alone = results["resolve"]
     hidden_off = 1.0 - (results["off"] - results["compute"]) / alone
     hidden_on = 1.0 - (results["on"] - results["compute"]) / alone
-    shared = sum(1 for l in range(NL) if w.anchors[l] != l)
     return {
         "metric": "resolve time hidden behind compute: step time with and without resolves",
         "value": hidden_on, "unit": "fraction of the resolves' own time hidden (prefetch on)",
@@ -736,7 +1122,10 @@ def run_prefetch_overlap(args, w):
         "prefetch_gain": 1.0 - (results["on"] - results["compute"]) /
                          (results["off"] - results["compute"]),
         "higher_is_better": True,
-        "config": {"workload": workload_name(w), "shared_layers_per_step": shared,
+        "config": {"workload": workload_name(w), "shared_layers_per_step": len(shared),
+                   "prefetch_source": ("the anchor's miss plan written by its resolve "
+                                       "(hs_resolve_anchor)" if replay else
+                                       "hs_prefetch_plan per shared layer"),
                    "attention": (f"hs_sparse_attention over the published slots, {heads} "
                                  f"heads per request" if attn else "none"),
                    "mlp_stand_in": f"bf16 GEMM 4096x4096x{n} after every layer",
@@ -750,7 +1139,7 @@ def run_prefetch_overlap(args, w):
     }
 
 
-def time_prefetch_kernels(pool, w, dsel, out, plans, flush, stream, args):
+def time_prefetch_kernels(pool, w, dsel, out, plans, flush, stream, args, replay=False):
     """The plan and copy kernels of exact prefetch, each timed alone.
 
     The same decode steps as prefetch ON, all on one stream and without the
@@ -771,22 +1160,29 @@ def time_prefetch_kernels(pool, w, dsel, out, plans, flush, stream, args):
     R, NL, k, B, W, T = w.n_requests, w.n_layers, w.k, w.slots, w.record_bytes, w.steps
     h2d_gbs, _ = hs.hs_link_probe(1 << 30, 10, W)
 
+    shared = [l for l in range(NL) if w.anchors[l] != l]
+
     def step(t, pending):
         for l in range(NL):
             if w.anchors[l] == l:
-                pool.resolve(l, dsel[t, l], out[l], stream=stream)
-                for l2 in plans:
+                if replay and l in plans:
+                    pool.resolve_anchor(l, dsel[t, l], out[l], plans[l], stream=stream)
+                else:
+                    pool.resolve(l, dsel[t, l], out[l], stream=stream)
+                for l2 in shared:
                     if w.anchors[l2] != l:
                         continue
                     ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
                     ev[0].record(stream)
-                    pool.prefetch_plan(l, l2, dsel[t, l2], plans[l2], stream=stream)
+                    if not replay:
+                        pool.prefetch_plan(l, l2, dsel[t, l2], plans[l2], stream=stream)
                     ev[1].record(stream)
-                    pool.prefetch_copy(l2, R, k, plans[l2], stream=stream)
+                    pool.prefetch_copy(l2, R, k, plans[l if replay else l2], stream=stream)
                     ev[2].record(stream)
                     pending.append(ev)
             else:
-                pool.resolve(l, dsel[t, l], out[l], plan=plans[l], stream=stream)
+                pool.resolve(l, dsel[t, l], out[l], plan=plans[w.anchors[l] if replay else l],
+                             stream=stream)
 
     pool.reset()
     for s in range(args.warmup):
@@ -812,13 +1208,13 @@ def time_prefetch_kernels(pool, w, dsel, out, plans, flush, stream, args):
     plan_bytes = calls * (R * (4 * k + 6 * B + 16) + 16) + 8 * planned
     peaks = load_peaks()
     hbm = peaks.get("hbm_gbs") if peaks else None
-    plan_gbs = plan_bytes / (plan_ms / 1e3) / 1e9
+    plan_gbs = plan_bytes / (plan_ms / 1e3) / 1e9 if not replay and plan_ms > 0 else None
     copy_gbs = moved / (copy_ms / 1e3) / 1e9
     return {
         "calls": calls,
         "requests_per_call": R,
         "records_per_call": planned / calls,
-        "plan": {"us_per_call": plan_ms * 1e3 / calls, "kernels_per_call": 1,
+        "plan": None if replay else {"us_per_call": plan_ms * 1e3 / calls, "kernels_per_call": 1,
                  "algorithmic_bytes_per_call": plan_bytes / calls,
                  "roofline": {"bound": "hbm", "achieved": plan_gbs, "peak": hbm,
                               "unit": "GB/s", "frac": plan_gbs / hbm if hbm else None,
@@ -940,14 +1336,117 @@ def run_attention(args, w):
 
 # ------------------------------------------------------------------ main ----
 
+def link_sweep(sizes_gib, record_bytes: int) -> dict:
+    """hs_link_probe over host buffers of each size, for each allocation
+    kind: the pinned H2D copy rate (1 GiB from the buffer's start) and the
+    rate of gathering 1 GiB of `record_bytes` records from indices spread
+    uniformly over the whole buffer -- where scattered GPU-thread reads of a
+    pool of that size stand against the link (best of 3 each)."""
+    from hierarchical_kv_cache_resolve_gb300 import hs
+    rows = []
+    for gib in sizes_gib:
+        for name in ("pinned", "vmm"):
+            t0 = time.perf_counter()
+            try:
+                h2d, gather = hs.hs_link_probe(gib << 30, 3, record_bytes, HOST_ALLOC[name])
+                rows.append({"gib": gib, "host_alloc": name, "h2d_gbs": h2d,
+                             "gather_gbs": gather, "s": time.perf_counter() - t0})
+            except hs.HsError as e:
+                rows.append({"gib": gib, "host_alloc": name, "error": str(e)})
+    return {"what": "hs_link_probe per host allocation kind and buffer size", "unit": "GB/s",
+            "record_bytes": record_bytes, "rows": rows}
+
+
+def spawn_ranks(n: int, argv) -> int:
+    """`bench.py --gpus N` started as one process: re-run it under
+    torch.distributed.run with one rank per GPU on this node (rendezvous on
+    127.0.0.1), and return the launcher's exit status.  Rank 0 prints the
+    JSON line."""
+    import socket
+    import subprocess
+    with socket.socket() as so:
+        so.bind(("127.0.0.1", 0))
+        port = so.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={n}", "--master-addr=127.0.0.1", f"--master-port={port}",
+           os.path.abspath(__file__)] + list(argv)
+    return subprocess.call(cmd)
+
+
+def bind_to_device_numa(device: int):
+    """Runs this process on the CPUs of the host NUMA node closest to
+    `device` (cudaDevAttrHostNumaId), so the records it generates are
+    written by local cores; returns (node, cpus) or (None, None) when the
+    system reports no node for the device.  The pool's pinned pages are
+    placed on that node by the library itself (hs_create_pool)."""
+    from hierarchical_kv_cache_resolve_gb300 import hs
+    node = hs.hs_device_host_numa(device)
+    if node < 0:
+        return None, None
+    try:
+        with open(f"/sys/devices/system/node/node{node}/cpulist") as f:
+            cpus = parse_cpulist(f.read())
+        cpus &= os.sched_getaffinity(0) or cpus
+        if cpus:
+            os.sched_setaffinity(0, cpus)
+        return node, len(cpus)
+    except OSError:
+        return node, None
+
+
+def parse_cpulist(text: str) -> set:
+    """'0-3,8,10-11' -> {0, 1, 2, 3, 8, 10, 11}"""
+    cpus = set()
+    for part in text.strip().split(","):
+        if not part:
+            continue
+        if "-" in part:
+            a, b = part.split("-")
+            cpus.update(range(int(a), int(b) + 1))
+        else:
+            cpus.add(int(part))
+    return cpus
+
+
+def reference_arm(args, w, threads: int) -> dict:
+    """The reference arm: the CPU oracle as it stands on a bounded sample of
+    the workload (the first CPU_SAMPLE_PAIRS (request, layer) pairs, each
+    over warm-up + timed steps of its trace, one thread per pair)."""
+    pairs = min(w.n_requests * w.n_layers, CPU_SAMPLE_PAIRS)
+    steps = args.warmup + args.steps
+    value, wall, n, fetched = time_oracle(w, pairs, steps, threads)
+    sample = (f"the CPU oracle on {pairs} of the {w.n_requests * w.n_layers} (request, layer) "
+              f"pairs x {steps} steps (warm-up included), one thread per pair, "
+              f"{min(threads, pairs)} threads")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "resolves/s",
+            "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": wall / steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "int32", "data": "synthetic",
+            "config": {"workload": workload_name(w), "global_batch": w.n_requests,
+                       "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "resolves/s", "cores": min(threads, pairs),
+                             "kind": "oracle", "sample": sample, "cpu_model": cpu_model()},
+            "e2e": {"value": value, "unit": "resolves/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "miss_fetch": {"gbs": fetched / wall / 1e9, "unit": "GB/s"}}
+
+
 def main(argv=None):
+    argv = sys.argv[1:] if argv is None else list(argv)
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1024)
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="dsa_mla")
+    ap.add_argument("--workload", default="tight_prefetch",
+                    help="the headline workload (default: the largest, tight_prefetch)")
+    ap.add_argument("--also", default="dsa_mla",
+                    help="comma-separated workloads timed after the headline (graph pass "
+                         "only) and reported beside it; 'none' for none")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--host-alloc", choices=sorted(HOST_ALLOC), default="auto",
+                    help="how the pinned host pool is allocated (hs_pool_desc.host_alloc)")
     ap.add_argument("--cpu-threads", type=int, default=0)
     ap.add_argument("--l-ctx", type=int, default=0,
                     help="profiling captures only: shrink L_ctx (same k, B, W, batch), so "
@@ -957,51 +1456,49 @@ def main(argv=None):
     ap.add_argument("--prefetch-overlap", action="store_true",
                     help="measure exact layer-wise prefetch against stand-in compute "
                          "(a workload with shared layers, e.g. tight_prefetch)")
+    ap.add_argument("--prefetch-source", choices=["replay", "plan"], default="replay",
+                    help="--prefetch-overlap: the anchor's own miss plan (hs_resolve_anchor) "
+                         "or one hs_prefetch_plan launch per shared layer")
     ap.add_argument("--compute-us", type=float, default=60.0,
                     help="MLP stand-in compute per layer for --prefetch-overlap")
     ap.add_argument("--attention", action="store_true",
                     help="time the sparse attention consumer alone on the workload's shape")
+    ap.add_argument("--link-sweep", default="",
+                    help="comma-separated GiB sizes: time hs_link_probe (pinned H2D copy and "
+                         "scattered record gather over the whole buffer) for each host "
+                         "allocation kind and size, print one JSON line, and exit")
     ap.add_argument("--attn-heads", type=int, default=16,
                     help="query heads per request of the sparse attention consumer in "
                          "--prefetch-overlap (a multiple of 16; 0: no attention)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.gpus < 1:
+        ap.error("--gpus must be at least 1")
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        return spawn_ranks(args.gpus, argv)
 
     from workloads import configs
-    base = configs.BY_NAME[args.workload]
-    if args.l_ctx:
-        base = base.with_(n_positions=args.l_ctx,
-                          local_window=min(base.local_window, args.l_ctx // 8))
-    if args.requests:
-        base = base.with_(n_requests=args.requests)
+
+    def shaped(name):
+        w = configs.BY_NAME[name]
+        if args.l_ctx:
+            w = w.with_(n_positions=args.l_ctx, local_window=min(w.local_window, args.l_ctx // 8))
+        if args.requests:
+            w = w.with_(n_requests=args.requests)
+        return w
+
+    base = shaped(args.workload)
+    also = [] if args.also in ("", "none") else [x for x in args.also.split(",")
+                                                  if x and x != args.workload]
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     threads = args.cpu_threads or len(os.sched_getaffinity(0))
 
     if args.impl == "reference":
-        if rank != 0:
-            return 0
-        w = base
-        value, wall, n, fetched = time_oracle(w, w.n_requests * w.n_layers,
-                                              args.warmup + args.steps, threads)
-        res = {"impl": "reference", "metric": METRIC, "value": value, "unit": "resolves/s",
-               "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
-               "ms_per_step": wall / (args.warmup + args.steps) * 1e3,
-               "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-               "dtype": "int32", "data": "synthetic",
-               "config": {"workload": workload_name(w), "global_batch": w.n_requests},
-               "cpu_baseline": {"value": value, "unit": "resolves/s", "cores": threads,
-                                "kind": "oracle",
-                                "sample": (f"the CPU oracle on all {w.n_requests * w.n_layers} "
-                                           f"(request, layer) pairs x "
-                                           f"{args.warmup + args.steps} steps, one thread per "
-                                           f"pair, {threads} threads; warm-up included")},
-               "e2e": {"value": value, "unit": "resolves/s", "h2d_bytes_per_step": 0,
-                       "d2h_bytes_per_step": 0},
-               "miss_fetch": {"gbs": fetched / wall / 1e9, "unit": "GB/s"}}
-        print(json.dumps(res))
+        if rank == 0:
+            print(json.dumps(reference_arm(args, base, threads)))
         return 0
 
     import torch
@@ -1009,9 +1506,15 @@ def main(argv=None):
     if not torch.cuda.is_available():
         raise SystemExit("bench.py: no CUDA device (the resolve path has no CPU fallback)")
     torch.cuda.set_device(local)
+    numa, numa_cpus = bind_to_device_numa(local)
     if dist_on:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if args.link_sweep:
+        if rank == 0:
+            print(json.dumps(link_sweep([int(x) for x in args.link_sweep.split(",") if x],
+                                        base.record_bytes)))
+        return 0
     w = rank_workload(base, rank)
     if args.prefetch_overlap or args.attention:
         if rank == 0:
@@ -1019,6 +1522,14 @@ def main(argv=None):
             print(json.dumps(run(args, w)))
         return 0
     res = run_gpu(args, w, rank, world, dist_on)
+    res["config"]["host_numa_node"] = numa
+    res["config"]["process_cpus"] = numa_cpus
+    others = {}
+    for name in also:
+        lite = run_gpu(args, rank_workload(shaped(name), rank), rank, world, dist_on, lite=True)
+        others[name] = lite
+    if others:
+        res["other_workloads"] = others
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
             res["cpu_baseline"] = cpu_baseline(base, threads)

@@ -51,8 +51,13 @@ def _load():
     global _lib
     with _lock:
         if _lib is None:
-            build()
-            lib = ctypes.CDLL(_LIB)
+            # a separately built copy (e.g. the sanitizer build of the
+            # tests) may be named in the environment
+            path = os.environ.get("HS_ORACLE_LIB")
+            if not path:
+                build()
+                path = _LIB
+            lib = ctypes.CDLL(path)
             P = ctypes.POINTER(_PairC)
             vp, i32 = ctypes.c_void_p, ctypes.c_int32
             lib.ora_validate.argtypes = [P, vp, i32]

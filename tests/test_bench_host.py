@@ -97,7 +97,8 @@ def test_reference_arm_json(capsys):
     line = capsys.readouterr().out.strip().splitlines()[-1]
     d = json.loads(line)
     assert d["impl"] == "reference" and d["unit"] == "resolves/s" and d["value"] > 0
-    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 2
+    # tiny has one (request, layer) pair: one of the two threads does the work
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["higher_is_better"] is True
 
 
@@ -111,3 +112,30 @@ def test_gpu_arm_refuses_without_cuda():
         pytest.skip("a GPU is present")
     with pytest.raises(SystemExit):
         bench.main(["--steps", "3", "--warmup", "3"])
+
+
+def test_gpus_flag_spawns_one_process_per_rank(capfd, monkeypatch):
+    """`bench.py --gpus 2` run as a single process re-runs itself under
+    torch.distributed.run with two ranks (rendezvous on 127.0.0.1); rank 0
+    prints the one JSON line and both exit 0 (here through the reference
+    arm, which needs no GPU)."""
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    rc = bench.main(["--impl", "reference", "--workload", "tiny", "--gpus", "2", "--steps", "4",
+                     "--warmup", "3", "--cpu-threads", "1"])
+    assert rc == 0
+    out = capfd.readouterr().out
+    lines = [x for x in out.splitlines() if x.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0
+
+
+def test_parse_cpulist():
+    assert bench.parse_cpulist("0-3,8,10-11\n") == {0, 1, 2, 3, 8, 10, 11}
+    assert bench.parse_cpulist("") == set()
+
+
+def test_bind_without_device_reports_no_node():
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert bench.bind_to_device_numa(0) == (None, None)

@@ -24,7 +24,8 @@ def test_default_bench_line():
     assert d["unit"] == "resolves/s" and d["value"] > 0 and d["higher_is_better"] is True
     assert d["n_gpus"] == 1 and d["steps"] == 8 and d["warmup"] == 3
     assert d["scaling"] == "weak" and d["data"] == "synthetic" and d["dtype"] == "int32"
-    assert d["config"]["workload"].startswith("dsa_mla")
+    assert d["config"]["workload"].startswith("tight_prefetch")   # the largest workload
+    layers = 8
     # value = resolves of the timed steps over their device time
     resolves = d["config"]["resolves_per_step"] * d["steps"]
     assert abs(d["value"] - resolves / (d["ms_per_step"] * d["steps"] / 1e3)) <= 1e-6 * d["value"]
@@ -39,5 +40,14 @@ def test_default_bench_line():
     e = d["e2e"]
     assert e["unit"] == "resolves/s" and 0 < e["value"]
     assert e["h2d_bytes_per_step"] == e["d2h_bytes_per_step"] == resolves // d["steps"] * 2048 * 4
-    assert d["gpu_launches"] == d["steps"] * 4       # four layers, one launch each
+    assert d["gpu_launches"] == d["steps"] * layers   # one launch per layer
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
+    # exact prefetch beside the value: every plan pair matched, nothing lost
+    p = d["prefetch_on"]
+    assert p["status"] == 0 and p["counters"]["plan_mismatches"] == 0
+    assert p["counters"]["resolves"] == resolves
+    assert p["counters"]["plan_hits"] * 1152 == p["counters"]["prefetched_bytes"]
+    assert d["copy_only"]["status"] == 0 and d["copy_only"]["link_gbs"] > 0
+    assert d["no_fetch"]["status"] == 0 and d["stages"]["status"] == 0
+    assert d["no_fetch"]["roofline_hbm_metadata"]["bound"] == "hbm"
+    assert "dsa_mla" in d["other_workloads"]

@@ -38,8 +38,13 @@ def _load():
     global _lib
     with _lock:
         if _lib is None:
-            build()
-            lib = ctypes.CDLL(_LIB)
+            # a separately built copy (e.g. the sanitizer build of the
+            # tests) may be named in the environment
+            path = os.environ.get("HS_RECORDS_LIB")
+            if not path:
+                build()
+                path = _LIB
+            lib = ctypes.CDLL(path)
             lib.wl_gen_records.argtypes = [
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32,
                 ctypes.c_int, ctypes.c_uint64, ctypes.c_uint64]

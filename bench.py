@@ -53,6 +53,7 @@ METRIC = ("resolves/sec and miss-fetch GB/s (fraction of measured pinned H2D BW)
           "at 1 GB300")
 L2_FLUSH_BYTES = 256 << 20
 HOST_ALLOC = {"auto": 0, "pinned": 1, "vmm": 2}
+OVERLAP = {"auto": 0, "on": 1, "off": 2}
 CONT_STEPS, CONT_BLOCKS = 16, 3
 
 # Counters of one steady-state resolve launch from an ncu capture (dsa_mla
@@ -378,7 +379,7 @@ def run_gpu(args, w, rank, world, dist_on, lite=False):
     sel = traces.generate(w)
     dsel = torch.from_numpy(np.ascontiguousarray(sel.transpose(0, 2, 1, 3))).to(dev)
     t_fill = time.perf_counter()
-    pool = hs.Pool.for_workload(w, host_alloc=kind)
+    pool = hs.Pool.for_workload(w, host_alloc=kind, launch_overlap=OVERLAP[args.launch_overlap])
     pool_info = pool.info()
     for r in range(R):
         for l in range(NL):
@@ -602,7 +603,8 @@ def run_gpu(args, w, rank, world, dist_on, lite=False):
             "global_batch": R * world,
             "resolves_per_step": R * NL * world,
             "parallelism": f"requests sharded, {world} independent pool(s), no collective",
-            "launch": f"per-step CUDA graph of {NL} hs_resolve launches",
+            "launch": (f"per-step CUDA graph of {NL} hs_resolve launches, launch overlap "
+                       f"{'on' if pool_info['launch_overlap'] == 1 else 'off'}"),
             "l2": "flushed before every timed step (256 MiB write + 256 MiB read, outside the events)",
             "record_values": "bf16 N(0,1)" if w.value_format else "fp16 U(-1,1)",
         },
@@ -865,6 +867,8 @@ def summarise_stamps(a, C):
             d["leader_start"] = (ld[S["ENTRY"]] - t0) / 1e3
             d["decision_done"] = (ld[S["DECIDED"]] - t0) / 1e3
             d["commit_done"] = (ld[S["COMMITTED"]] - t0) / 1e3
+            d["leader_share_fetched"] = ((ld[S["LEAD_FETCHED"]] - t0) / 1e3
+                                         if ld[S["LEAD_FETCHED"]] > 0 else None)
             d["launch_span"] = span / 1e3
             d["attempts"] = ld[S["ATTEMPTS"]]
             if C > 1:
@@ -1447,6 +1451,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--host-alloc", choices=sorted(HOST_ALLOC), default="auto",
                     help="how the pinned host pool is allocated (hs_pool_desc.host_alloc)")
+    ap.add_argument("--launch-overlap", choices=sorted(OVERLAP), default="auto",
+                    help="whether consecutive resolves may overlap (hs_pool_desc.launch_overlap)")
     ap.add_argument("--cpu-threads", type=int, default=0)
     ap.add_argument("--l-ctx", type=int, default=0,
                     help="profiling captures only: shrink L_ctx (same k, B, W, batch), so "
@@ -1521,13 +1527,15 @@ def main(argv=None):
             run = run_prefetch_overlap if args.prefetch_overlap else run_attention
             print(json.dumps(run(args, w)))
         return 0
-    res = run_gpu(args, w, rank, world, dist_on)
-    res["config"]["host_numa_node"] = numa
-    res["config"]["process_cpus"] = numa_cpus
+    # the smaller workloads first: their pools are allocated before the
+    # headline's large one has been pinned and freed
     others = {}
     for name in also:
         lite = run_gpu(args, rank_workload(shaped(name), rank), rank, world, dist_on, lite=True)
         others[name] = lite
+    res = run_gpu(args, w, rank, world, dist_on)
+    res["config"]["host_numa_node"] = numa
+    res["config"]["process_cpus"] = numa_cpus
     if others:
         res["other_workloads"] = others
     if rank == 0:

@@ -100,13 +100,13 @@ class PoolDesc(ctypes.Structure):
                 ("n_positions", ctypes.c_int64), ("record_bytes", ctypes.c_int32),
                 ("slots", ctypes.c_int32), ("max_k", ctypes.c_int32),
                 ("layer_anchor", ctypes.c_void_p), ("host_limit_bytes", ctypes.c_uint64),
-                ("host_alloc", ctypes.c_int32)]
+                ("host_alloc", ctypes.c_int32), ("launch_overlap", ctypes.c_int32)]
 
 
 class PoolInfo(ctypes.Structure):
     _fields_ = [("host_alloc", ctypes.c_int32), ("device", ctypes.c_int32),
                 ("device_numa", ctypes.c_int32), ("host_numa_first", ctypes.c_int32),
-                ("host_numa_last", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("host_numa_last", ctypes.c_int32), ("launch_overlap", ctypes.c_int32),
                 ("host_bytes", ctypes.c_uint64), ("host_mapped_bytes", ctypes.c_uint64),
                 ("host_granularity", ctypes.c_uint64), ("device_bytes", ctypes.c_uint64)]
 

@@ -17,6 +17,7 @@ struct hs_pool {
     int device = 0;
     int sm_count = 0;
     int cluster_override = 0;
+    bool overlap = true;  // consecutive resolves may overlap (launch_overlap)
     hs::HostBuffer host = {};
     size_t host_bytes = 0;
     hs::DevPool dp = {};
@@ -68,6 +69,14 @@ int pick_cluster(const hs_pool *p, int n_req) {
     return c;
 }
 
+// Selections whose misses the leader CTA fetches itself: without launch
+// overlap its decision is never hidden under an earlier launch, and it
+// would otherwise idle while its followers move the records; it takes an
+// equal share of the selection.
+int lead_share(const hs_pool *p, int k, int cluster) {
+    return (p->overlap || cluster < 2) ? 0 : k / cluster;
+}
+
 bool check_common(const hs_pool *p, int32_t layer, int32_t n_req, int32_t k) {
     return p && layer >= 0 && layer < p->desc.n_layers && n_req >= 0 &&
            n_req <= p->desc.n_requests && k >= 1 && k <= p->desc.max_k;
@@ -85,7 +94,7 @@ static_assert(HS_STAMP_ENTRY == hs::S_ENTRY && HS_STAMP_LOADED == hs::S_LOADED &
                   HS_STAMP_F_ISSUE == hs::S_F_ISSUE && HS_STAMP_F_ISSUED == hs::S_F_ISSUED &&
                   HS_STAMP_F_WAITED == hs::S_F_WAITED && HS_STAMP_F_LANDED == hs::S_F_LANDED &&
                   HS_STAMP_F_STORED == hs::S_F_STORED && HS_STAMP_ATTEMPTS == hs::S_ATTEMPTS &&
-                  HS_STAMP_EXIT == hs::S_EXIT,
+                  HS_STAMP_EXIT == hs::S_EXIT && HS_STAMP_LEAD_FETCHED == hs::S_LEAD_FETCHED,
               "stamp slots of hs.h and the kernel differ");
 
 extern "C" {
@@ -118,7 +127,8 @@ int hs_create_pool(const hs_pool_desc *desc, hs_pool **out) {
     if (d.n_requests < 1 || d.n_layers < 1 || d.n_positions < 1 ||
         d.n_positions > INT32_MAX || d.record_bytes < 16 || d.record_bytes % 16 != 0 ||
         d.slots < 1 || d.slots > 32767 || d.max_k < 1 || d.max_k > d.slots ||
-        d.host_alloc < HS_HOST_ALLOC_AUTO || d.host_alloc > HS_HOST_ALLOC_VMM_NUMA)
+        d.host_alloc < HS_HOST_ALLOC_AUTO || d.host_alloc > HS_HOST_ALLOC_VMM_NUMA ||
+        d.launch_overlap < HS_OVERLAP_AUTO || d.launch_overlap > HS_OVERLAP_OFF)
         return HS_ERR_INVALID_ARG;
     // index arithmetic limits of the kernels (32-bit chunk counters and
     // published row indices)
@@ -151,6 +161,9 @@ int hs_create_pool(const hs_pool_desc *desc, hs_pool **out) {
     p->desc.layer_anchor = p->anchor.data();
     p->device = dev;
     p->sm_count = sms;
+    p->overlap = d.launch_overlap == HS_OVERLAP_ON ||
+                 (d.launch_overlap == HS_OVERLAP_AUTO && host_bytes <= HS_OVERLAP_AUTO_MAX_HOST_BYTES);
+    p->desc.launch_overlap = p->overlap ? HS_OVERLAP_ON : HS_OVERLAP_OFF;
     if (const char *e = std::getenv("HS_CLUSTER")) {
         const int c = std::atoi(e);
         if (c == 1 || c == 2 || c == 4 || c == 8) p->cluster_override = c;
@@ -231,6 +244,7 @@ int hs_pool_info(hs_pool *pool, hs_pool_info_t *out) {
     std::memset(out, 0, sizeof(*out));
     out->host_alloc = pool->host.kind;
     out->device = pool->device;
+    out->launch_overlap = pool->desc.launch_overlap;
     out->device_numa = hs::device_host_numa(pool->device);
     const uint8_t *h = static_cast<const uint8_t *>(pool->host.host);
     out->host_numa_first = hs::page_numa_node(h);
@@ -263,9 +277,11 @@ int hs_resolve(hs_pool *pool, int32_t layer, int32_t n_req, const int32_t *d_req
     if (d_plan && (reinterpret_cast<uintptr_t>(d_plan) & 15u)) return HS_ERR_INVALID_ARG;
     if (misaligned4(d_sel) || misaligned4(d_out) || misaligned4(d_req_ids)) return HS_ERR_INVALID_ARG;
     if (n_req == 0) return HS_OK;
+    const int cluster = pick_cluster(pool, n_req);
     const cudaError_t e = hs::launch_resolve(pool->dp, layer, n_req, d_req_ids, d_sel, k, d_out, d_plan,
-                                             pick_cluster(pool, n_req), static_cast<cudaStream_t>(stream),
-                                             pool->anchor[layer]);
+                                             cluster, static_cast<cudaStream_t>(stream),
+                                             pool->anchor[layer], nullptr, pool->overlap,
+                                             lead_share(pool, k, cluster));
     return cuda_ok(e) ? HS_OK : HS_ERR_CUDA;
 }
 
@@ -278,9 +294,11 @@ int hs_resolve_anchor(hs_pool *pool, int32_t layer, int32_t n_req, const int32_t
         misaligned4(d_req_ids))
         return HS_ERR_INVALID_ARG;
     if (n_req == 0) return HS_OK;
+    const int cluster = pick_cluster(pool, n_req);
     const cudaError_t e = hs::launch_resolve(pool->dp, layer, n_req, d_req_ids, d_sel, k, d_out,
-                                             nullptr, pick_cluster(pool, n_req),
-                                             static_cast<cudaStream_t>(stream), -1, d_plan_out);
+                                             nullptr, cluster, static_cast<cudaStream_t>(stream),
+                                             -1, d_plan_out, pool->overlap,
+                                             lead_share(pool, k, cluster));
     return cuda_ok(e) ? HS_OK : HS_ERR_CUDA;
 }
 
@@ -292,10 +310,11 @@ int hs_resolve_measure(hs_pool *pool, int32_t layer, int32_t n_req, const int32_
         (reinterpret_cast<uintptr_t>(d_times) & 7u) || (flags & ~HS_MEASURE_NO_FETCH))
         return HS_ERR_INVALID_ARG;
     if (n_req == 0) return HS_OK;
+    const int cluster = pick_cluster(pool, n_req);
     const cudaError_t e = hs::launch_resolve_measure(
         pool->dp, layer, n_req, d_req_ids, d_sel, k, d_out, (flags & HS_MEASURE_NO_FETCH) != 0,
-        reinterpret_cast<unsigned long long *>(d_times), pick_cluster(pool, n_req),
-        static_cast<cudaStream_t>(stream));
+        reinterpret_cast<unsigned long long *>(d_times), cluster,
+        static_cast<cudaStream_t>(stream), pool->overlap, lead_share(pool, k, cluster));
     return cuda_ok(e) ? HS_OK : HS_ERR_CUDA;
 }
 
@@ -324,7 +343,7 @@ int hs_prefetch_copy(hs_pool *pool, int32_t target_layer, int32_t n_req, int32_t
     if (n_req == 0) return HS_OK;
     const cudaError_t e = hs::launch_prefetch_copy(pool->dp, target_layer, n_req, k, d_plan,
                                                    pool->sm_count, static_cast<cudaStream_t>(stream),
-                                                   pool->anchor[target_layer]);
+                                                   pool->anchor[target_layer], !pool->overlap);
     return cuda_ok(e) ? HS_OK : HS_ERR_CUDA;
 }
 

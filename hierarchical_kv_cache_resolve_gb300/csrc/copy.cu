@@ -123,14 +123,24 @@ __global__ void __launch_bounds__(kThreads)
 
 }  // namespace
 
+// Dynamic shared memory a confined copy asks for (unused by the kernel):
+// more than half of an SM's, so that no two of its CTAs share an SM.
+constexpr int kConfinedSmem = 120 * 1024;
+
+cudaError_t prepare_copy_kernel() {
+    return cudaFuncSetAttribute(prefetch_copy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kConfinedSmem);
+}
+
 cudaError_t launch_prefetch_copy(const DevPool &p, int layer, int n_req, int k, const void *plan,
-                                 int sm_count, cudaStream_t st, int plan_layer) {
-    // about two CTAs per SM in total, at least one per request row
-    int x = (2 * sm_count + n_req - 1) / n_req;
+                                 int sm_count, cudaStream_t st, int plan_layer, bool confined) {
+    // about two CTAs per SM in total, at least one per request row; or,
+    // confined, one CTA per SM and every SM on one request's records
+    int x = confined ? sm_count / n_req : (2 * sm_count + n_req - 1) / n_req;
     const int max_x = (k * (p.W >> 4) + kThreads - 1) / kThreads;
     if (x > max_x) x = max_x;
     if (x < 1) x = 1;
-    prefetch_copy_kernel<<<dim3(x, n_req), kThreads, 0, st>>>(
+    prefetch_copy_kernel<<<dim3(x, n_req), kThreads, confined ? kConfinedSmem : 0, st>>>(
         p, layer, n_req, k, static_cast<const uint8_t *>(plan), plan_layer);
     return cudaGetLastError();
 }

@@ -188,6 +188,7 @@ enum Stamp : int {
     S_F_STORED = 12,  // follower: slot stores and unstaged fetches issued
     S_ATTEMPTS = 13,  // leader: decisions taken (a count, not a time)
     S_EXIT = 14,      // both: last instruction
+    S_LEAD_FETCHED = 15,  // leader: its own share's misses fetched (launch overlap off)
 };
 
 // header word indices (u32 at smem + hdr)
@@ -205,6 +206,7 @@ enum Hdr : int {
     H_NX = 10,       // follower: leader misses it did not predict
     H_NSTG = 11,     // follower: staging slots handed out (may exceed the capacity)
     H_PSTAT = 12,    // plan-mode status bits, applied at the commit
+    H_NL = 13,       // leader: misses of its own fetch share
     H_SUMS = 16,     // kWarps scan sums from here
 };
 
@@ -228,21 +230,28 @@ int page_numa_node(const void *addr);
 // launchers (resolve.cu, copy.cu, attention.cu, attention_heads.cu)
 // plan_layer: a consumed plan may carry this layer id besides `layer` (the
 // anchor whose resolve wrote it); plan_out: where an anchor's resolve
-// writes its own miss plan (NULL: nowhere).
+// writes its own miss plan (NULL: nowhere); overlap: the launch may start
+// under the previous grid in the stream (programmatic stream
+// serialisation); lead_k: the leader CTA fetches the misses among the last
+// lead_k selections itself, the followers the rest (0: followers only).
 cudaError_t launch_resolve(const DevPool &p, int layer, int n_req, const int32_t *req_ids,
                            const int32_t *sel, int k, int32_t *out, const void *plan,
                            int cluster, cudaStream_t st, int plan_layer = -1,
-                           void *plan_out = nullptr);
+                           void *plan_out = nullptr, bool overlap = true, int lead_k = 0);
 cudaError_t launch_plan(const DevPool &p, int layer, int n_req, const int32_t *req_ids,
                         const int32_t *sel, int k, void *plan, cudaStream_t st);
 cudaError_t launch_resolve_measure(const DevPool &p, int layer, int n_req, const int32_t *req_ids,
                                    const int32_t *sel, int k, int32_t *out, bool no_fetch,
-                                   unsigned long long *times, int cluster, cudaStream_t st);
+                                   unsigned long long *times, int cluster, cudaStream_t st,
+                                   bool overlap, int lead_k);
+// confined: every SM copies records of one request only (one CTA per SM,
+// sm_count / n_req CTAs per request), for pools past the translation reach
 cudaError_t launch_prefetch_copy(const DevPool &p, int layer, int n_req, int k,
                                  const void *plan, int sm_count, cudaStream_t st,
-                                 int plan_layer);
+                                 int plan_layer, bool confined);
 cudaError_t launch_init_lru(uint16_t *lru, int64_t pairs, int B, cudaStream_t st);
 cudaError_t prepare_kernels(size_t max_smem);
+cudaError_t prepare_copy_kernel();
 cudaError_t launch_attention(const void *q, const void *cache, int64_t cache_rows,
                              const int32_t *idx, int n_req, int k, int heads, float scale,
                              float *out, cudaStream_t st);

@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     resolve_kernel(DevPool p, int layer, int n_req, const int32_t *__restrict__ req_ids,
                    const int32_t *__restrict__ sel_g, int k, int32_t *__restrict__ out_g,
                    const uint8_t *__restrict__ plan_in, uint8_t *__restrict__ plan_out,
-                   unsigned long long *__restrict__ times, int plan_layer) {
+                   unsigned long long *__restrict__ times, int plan_layer, int lead_k) {
     constexpr bool kPlanOnly = kMode == kModePlan;
     constexpr bool kNoFetch = kMode == kModeNoFetch;
     extern __shared__ __align__(16) uint8_t smem[];
@@ -365,6 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 hdr[H_PMISS] = 0u;
                 hdr[H_PHIT] = 0u;
                 hdr[H_PSTAT] = 0u;
+                hdr[H_NL] = 0u;
                 if (!r_ok) {
                     a0 |= HS_STATUS_REQ_RANGE;
                 } else {
@@ -716,7 +717,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t *sbits = reinterpret_cast<uint32_t *>(smem + fl.sbits);
         uint8_t *stage = smem + fl.stage;
         const int nf = csize > 1 ? (int)csize - 1 : 1, f = (int)crank - 1;
-        const int i0 = (int)((int64_t)f * k / nf), i1 = (int)((int64_t)(f + 1) * k / nf);
+        // the followers share [0, k - lead_k); the leader fetches the rest
+        const int kf = k - lead_k;
+        const int i0 = (int)((int64_t)f * kf / nf), i1 = (int)((int64_t)(f + 1) * kf / nf);
         const int ns = i1 - i0;
         const int nblk = (ns + 31) >> 5;
         const int32_t *pt = p.pt + pair * p.L;
@@ -891,6 +894,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const bool plist = hdr[H_FLIST] != 0u;
                     fetch_records(host_pair, cache_pair, plist ? fpos : mpos,
                                   plist ? fslot : mslot, F, W, tid, kThreads);
+                } else if (!kNoFetch && csize > 1 && lead_k > 0 && !with_plan) {
+                    // The leader's own share of the selection, [k - lead_k, k),
+                    // fetched by this CTA once it has committed, while the
+                    // followers store what they staged of theirs: one more SM
+                    // on the request's records, with a single request's
+                    // records on each SM.  Its misses are compacted into the
+                    // hash table's index array (free since the probe, read by
+                    // no follower).
+                    int32_t *lp = reinterpret_cast<int32_t *>(smem + sl.kidx);
+                    int32_t *ls = lp + lead_k;
+                    for (int i = k - lead_k + tid; i < k; i += kThreads) {
+                        const int32_t hsl = hit_s[i];
+                        if (hsl <= -2) {
+                            const uint32_t x = atomicAdd(&hdr[H_NL], 1u);
+                            lp[x] = mpos[-2 - hsl];
+                            ls[x] = mslot[-2 - hsl];
+                        }
+                    }
+                    __syncthreads();
+                    const int nl = (int)hdr[H_NL];
+                    if (nl > 0) fetch_records(host_pair, cache_pair, lp, ls, nl, W, tid, kThreads);
+                    stamp(S_LEAD_FETCHED);
                 }
                 if (tid == 0) {
                     __threadfence();
@@ -936,7 +961,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             int32_t *xp = reinterpret_cast<int32_t *>(smem + fl.xp);  // misses not staged
             int32_t *xs = reinterpret_cast<int32_t *>(smem + fl.xs);
             const int nf = csize > 1 ? (int)csize - 1 : 1, f = (int)crank - 1;
-            const int i0 = (int)((int64_t)f * k / nf), i1 = (int)((int64_t)(f + 1) * k / nf);
+            const int kf = k - lead_k;
+            const int i0 = (int)((int64_t)f * kf / nf), i1 = (int)((int64_t)(f + 1) * kf / nf);
             const int ns = i1 - i0;
             const int nblk = (ns + 31) >> 5;
             // F1: the victim slot of each staged record (-1: the leader found
@@ -1036,7 +1062,7 @@ cudaError_t prepare_kernels(size_t max_smem) {
             cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)max_smem);
         if (e != cudaSuccess) return e;
     }
-    return cudaSuccess;
+    return prepare_copy_kernel();
 }
 
 namespace {
@@ -1049,7 +1075,8 @@ template <int kMode, bool kStamps>
 cudaError_t launch_variant(const DevPool &p, int layer, int n_req, const int32_t *req_ids,
                            const int32_t *sel, int k, int32_t *out, const void *plan,
                            unsigned long long *times, int cluster, cudaStream_t st,
-                           int plan_layer = -1, void *plan_out = nullptr) {
+                           int plan_layer = -1, void *plan_out = nullptr, bool overlap = true,
+                           int lead_k = 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(n_req * cluster), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -1069,35 +1096,45 @@ cudaError_t launch_variant(const DevPool &p, int layer, int n_req, const int32_t
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].val.programmaticStreamSerializationAllowed = overlap ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
+    // the leader fetches a share of the selection only beside followers,
+    // and never from a plan (a consumed plan has its own fetch list)
+    if (cluster < 2 || plan != nullptr || lead_k < 0 || lead_k >= k) lead_k = 0;
     return cudaLaunchKernelEx(&cfg, resolve_kernel<kMode, kStamps>, p, layer, n_req, req_ids, sel,
                               k, out, static_cast<const uint8_t *>(plan),
-                              static_cast<uint8_t *>(plan_out), times, plan_layer);
+                              static_cast<uint8_t *>(plan_out), times, plan_layer, lead_k);
 }
 
 }  // namespace
 
 cudaError_t launch_resolve(const DevPool &p, int layer, int n_req, const int32_t *req_ids,
                            const int32_t *sel, int k, int32_t *out, const void *plan,
-                           int cluster, cudaStream_t st, int plan_layer, void *plan_out) {
+                           int cluster, cudaStream_t st, int plan_layer, void *plan_out,
+                           bool overlap, int lead_k) {
     return launch_variant<kModeResolve, false>(p, layer, n_req, req_ids, sel, k, out, plan,
-                                               nullptr, cluster, st, plan_layer, plan_out);
+                                               nullptr, cluster, st, plan_layer, plan_out, overlap,
+                                               lead_k);
 }
 
 cudaError_t launch_resolve_measure(const DevPool &p, int layer, int n_req, const int32_t *req_ids,
                                    const int32_t *sel, int k, int32_t *out, bool no_fetch,
-                                   unsigned long long *times, int cluster, cudaStream_t st) {
+                                   unsigned long long *times, int cluster, cudaStream_t st,
+                                   bool overlap, int lead_k) {
     if (no_fetch)
         return times ? launch_variant<kModeNoFetch, true>(p, layer, n_req, req_ids, sel, k, out,
-                                                          nullptr, times, cluster, st)
+                                                          nullptr, times, cluster, st, -1, nullptr,
+                                                          overlap, 0)
                      : launch_variant<kModeNoFetch, false>(p, layer, n_req, req_ids, sel, k, out,
-                                                           nullptr, nullptr, cluster, st);
+                                                           nullptr, nullptr, cluster, st, -1,
+                                                           nullptr, overlap, 0);
     return times ? launch_variant<kModeResolve, true>(p, layer, n_req, req_ids, sel, k, out,
-                                                      nullptr, times, cluster, st)
+                                                      nullptr, times, cluster, st, -1, nullptr,
+                                                      overlap, lead_k)
                  : launch_variant<kModeResolve, false>(p, layer, n_req, req_ids, sel, k, out,
-                                                       nullptr, nullptr, cluster, st);
+                                                       nullptr, nullptr, cluster, st, -1, nullptr,
+                                                       overlap, lead_k);
 }
 
 cudaError_t launch_plan(const DevPool &p, int layer, int n_req, const int32_t *req_ids,
@@ -1105,7 +1142,7 @@ cudaError_t launch_plan(const DevPool &p, int layer, int n_req, const int32_t *r
     const SmemLayout sl = smem_layout(p.B, k, false, p.L);
     resolve_kernel<kModePlan, false><<<n_req, kThreads, sl.total, st>>>(
         p, layer, n_req, req_ids, sel, k, nullptr, nullptr, static_cast<uint8_t *>(plan),
-        nullptr, -1);
+        nullptr, -1, 0);
     return cudaGetLastError();
 }
 

@@ -29,6 +29,10 @@ HS_HOST_ALLOC_AUTO = 0
 HS_HOST_ALLOC_PINNED = 1
 HS_HOST_ALLOC_VMM_NUMA = 2
 
+HS_OVERLAP_AUTO = 0
+HS_OVERLAP_ON = 1
+HS_OVERLAP_OFF = 2
+
 HS_STATUS_POS_RANGE = 0x1
 HS_STATUS_POS_DUP = 0x2
 HS_STATUS_REQ_RANGE = 0x4
@@ -86,13 +90,14 @@ def hs_plan_bytes(n_req: int, k: int) -> int:
 
 
 def hs_create_pool(n_requests, n_layers, n_positions, record_bytes, slots, max_k,
-                   layer_anchor=None, host_limit_bytes=0, host_alloc=HS_HOST_ALLOC_AUTO) -> int:
+                   layer_anchor=None, host_limit_bytes=0, host_alloc=HS_HOST_ALLOC_AUTO,
+                   launch_overlap=HS_OVERLAP_AUTO) -> int:
     anchors = None
     if layer_anchor is not None:
         anchors = (ctypes.c_int32 * len(layer_anchor))(*layer_anchor)
     d = _native.PoolDesc(n_requests, n_layers, n_positions, record_bytes, slots, max_k,
                          ctypes.cast(anchors, ctypes.c_void_p) if anchors is not None else None,
-                         host_limit_bytes, host_alloc)
+                         host_limit_bytes, host_alloc, launch_overlap)
     h = ctypes.c_void_p()
     _check(_lib().hs_create_pool(ctypes.byref(d), ctypes.byref(h)), "hs_create_pool")
     return h.value
@@ -122,7 +127,7 @@ def hs_device_host_numa(device: int) -> int:
 def hs_pool_info(pool: int) -> dict:
     i = _native.PoolInfo()
     _check(_lib().hs_pool_info(pool, ctypes.byref(i)), "hs_pool_info")
-    return {f: int(getattr(i, f)) for f, _ in _native.PoolInfo._fields_ if f != "reserved"}
+    return {f: int(getattr(i, f)) for f, _ in _native.PoolInfo._fields_}
 
 
 def hs_resolve(pool, layer, n_req, req_ids, sel, k, out, plan=None, stream=None) -> None:
@@ -137,7 +142,8 @@ def hs_resolve_anchor(pool, layer, n_req, req_ids, sel, k, out, plan_out, stream
 
 HS_MEASURE_NO_FETCH = 0x1
 HS_STAMPS = ("ENTRY", "LOADED", "HASHED", "PROBED", "DECIDED", "CHECKED", "VERDICT", "COMMITTED",
-             "F_ISSUE", "F_ISSUED", "F_WAITED", "F_LANDED", "F_STORED", "ATTEMPTS", "EXIT")
+             "F_ISSUE", "F_ISSUED", "F_WAITED", "F_LANDED", "F_STORED", "ATTEMPTS", "EXIT",
+             "LEAD_FETCHED")
 HS_STAMP = {name: i for i, name in enumerate(HS_STAMPS)}
 
 
@@ -250,16 +256,19 @@ class Pool:
     """A pool handle plus host and device views."""
 
     def __init__(self, n_requests, n_layers, n_positions, record_bytes, slots, max_k,
-                 layer_anchor=None, host_limit_bytes=0, host_alloc=HS_HOST_ALLOC_AUTO):
+                 layer_anchor=None, host_limit_bytes=0, host_alloc=HS_HOST_ALLOC_AUTO,
+                 launch_overlap=HS_OVERLAP_AUTO):
         self.R, self.NL, self.L = n_requests, n_layers, n_positions
         self.W, self.B, self.max_k = record_bytes, slots, max_k
         self.handle = hs_create_pool(n_requests, n_layers, n_positions, record_bytes, slots,
-                                     max_k, layer_anchor, host_limit_bytes, host_alloc)
+                                     max_k, layer_anchor, host_limit_bytes, host_alloc,
+                                     launch_overlap)
 
     @classmethod
-    def for_workload(cls, w, host_limit_bytes=0, host_alloc=HS_HOST_ALLOC_AUTO):
+    def for_workload(cls, w, host_limit_bytes=0, host_alloc=HS_HOST_ALLOC_AUTO,
+                     launch_overlap=HS_OVERLAP_AUTO):
         return cls(w.n_requests, w.n_layers, w.n_positions, w.record_bytes, w.slots, w.k,
-                   list(w.anchors), host_limit_bytes, host_alloc)
+                   list(w.anchors), host_limit_bytes, host_alloc, launch_overlap)
 
     def info(self) -> dict:
         return hs_pool_info(self.handle)

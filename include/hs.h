@@ -87,7 +87,30 @@ typedef struct {
     /* How the host pool is allocated: HS_HOST_ALLOC_* (0: the library's
        choice, see HS_HOST_ALLOC_AUTO). */
     int32_t host_alloc;
+    /* Whether consecutive resolves may overlap: HS_OVERLAP_* (0: the
+       library's choice, see HS_OVERLAP_AUTO). */
+    int32_t launch_overlap;
 } hs_pool_desc;
+
+/* ---- launch overlap (hs_pool_desc.launch_overlap) ---------------------- */
+/* ON: a resolve may start under the kernel ahead of it in the stream
+ * (programmatic dependent launch): it stages its predicted misses and
+ * takes its decision while that kernel finishes, and keeps the decision
+ * only if its inputs are unchanged once that kernel has completed.  Best
+ * while every host record stays within the device's translation reach:
+ * the reads of two or three layers' records then share it freely.
+ * OFF: each resolve starts when the kernel ahead of it has completed, so
+ * one layer's records are read at a time, and the leader CTA of each
+ * request fetches a share of the misses beside its followers.  Best for
+ * pools past the reach, where reads of several layers' records at once
+ * thrash the device's translations.
+ * AUTO: ON for pools of at most HS_OVERLAP_AUTO_MAX_HOST_BYTES of host
+ * records, OFF above (measured on GB300: the 59 GB pool of 64 requests x 8
+ * layers resolves 1.7x faster with OFF; 5 GB pools faster with ON). */
+#define HS_OVERLAP_AUTO 0
+#define HS_OVERLAP_ON 1
+#define HS_OVERLAP_OFF 2
+#define HS_OVERLAP_AUTO_MAX_HOST_BYTES (16ull << 30)
 
 /* ---- host pool memory (hs_pool_desc.host_alloc, hs_link_probe) --------- */
 /* The library's choice: HS_HOST_ALLOC_PINNED.  (Measured on GB300:
@@ -167,7 +190,7 @@ typedef struct {
     int32_t device_numa;       /* host NUMA node closest to that device, -1 unknown */
     int32_t host_numa_first;   /* NUMA node of the first page of the host pool, -1 unknown */
     int32_t host_numa_last;    /* NUMA node of its last page, -1 unknown */
-    int32_t reserved;
+    int32_t launch_overlap;    /* HS_OVERLAP_ON or HS_OVERLAP_OFF, as resolved */
     uint64_t host_bytes;       /* bytes of host records */
     uint64_t host_mapped_bytes;/* bytes allocated for them (granularity-rounded) */
     uint64_t host_granularity; /* VMM allocation granularity, 0 for cudaHostAlloc */
@@ -256,8 +279,9 @@ int hs_resolve(hs_pool *pool, int32_t layer, int32_t n_req, const int32_t *d_req
  * (metadata written) for the leader; F_ISSUE (first staging copy issued),
  * F_ISSUED (all issued), F_WAITED (previous grid complete), F_LANDED
  * (staged records in shared memory), F_STORED (slot stores and unstaged
- * fetches issued) for followers; ATTEMPTS holds the leader's count of
- * decisions, not a time. */
+ * fetches issued) for followers; LEAD_FETCHED (the leader's own share of
+ * misses fetched, when launch overlap is off) for the leader; ATTEMPTS
+ * holds the leader's count of decisions, not a time. */
 #define HS_STAMP_ENTRY 0
 #define HS_STAMP_LOADED 1
 #define HS_STAMP_HASHED 2
@@ -273,6 +297,7 @@ int hs_resolve(hs_pool *pool, int32_t layer, int32_t n_req, const int32_t *d_req
 #define HS_STAMP_F_STORED 12
 #define HS_STAMP_ATTEMPTS 13
 #define HS_STAMP_EXIT 14
+#define HS_STAMP_LEAD_FETCHED 15
 int hs_resolve_measure(hs_pool *pool, int32_t layer, int32_t n_req, const int32_t *d_req_ids,
                        const int32_t *d_sel, int32_t k, int32_t *d_out, int32_t flags,
                        uint64_t *d_times, void *stream);

@@ -46,7 +46,7 @@ def test_host_only_helpers(lib):
 
 def _desc(**kw):
     d = dict(n_requests=2, n_layers=2, n_positions=1000, record_bytes=128, slots=64,
-             max_k=32, layer_anchor=None, host_limit_bytes=0, host_alloc=0)
+             max_k=32, layer_anchor=None, host_limit_bytes=0, host_alloc=0, launch_overlap=0)
     d.update(kw)
     return _native.PoolDesc(**d)
 
@@ -54,7 +54,8 @@ def _desc(**kw):
 @pytest.mark.parametrize("bad", [
     dict(n_requests=0), dict(n_layers=0), dict(n_positions=0), dict(n_positions=1 << 31),
     dict(record_bytes=100), dict(record_bytes=0), dict(slots=0), dict(slots=40000),
-    dict(max_k=0), dict(max_k=65), dict(host_alloc=-1), dict(host_alloc=3)])
+    dict(max_k=0), dict(max_k=65), dict(host_alloc=-1), dict(host_alloc=3),
+    dict(launch_overlap=-1), dict(launch_overlap=3)])
 def test_create_pool_rejects_bad_descriptors(lib, bad):
     h = ctypes.c_void_p(1234)
     rc = lib.hs_create_pool(ctypes.byref(_desc(**bad)), ctypes.byref(h))

@@ -172,9 +172,12 @@ def test_shapes(shape):
                 for l in range(w.n_layers))
 
 
+@pytest.mark.parametrize("overlap", [hs.HS_OVERLAP_ON, hs.HS_OVERLAP_OFF])
 @pytest.mark.parametrize("cluster", ["1", "2", "4", "8"])
-def test_every_cluster_size(cluster, monkeypatch):
-    """Leader-only (1 CTA) and 1, 3, 7 followers give the same result."""
+def test_every_cluster_size(cluster, overlap, monkeypatch):
+    """Leader-only (1 CTA) and 1, 3, 7 followers give the same result, with
+    launch overlap and without it (then the leader also fetches the misses
+    of its own share of the selection)."""
     monkeypatch.setenv("HS_CLUSTER", cluster)
     w = _small(n_requests=4, k=300, slots=512, n_positions=5000, steps=12)
     sel = _random_trace(w, seed=17)
@@ -188,7 +191,8 @@ def test_every_cluster_size(cluster, monkeypatch):
                          if p not in keep][:150]
                 sel[t, r, l, 150:] = fresh
     orc = _oracles(w)
-    with hs.Pool.for_workload(w) as pool:
+    with hs.Pool.for_workload(w, launch_overlap=overlap) as pool:
+        assert pool.info()["launch_overlap"] == overlap
         fill_selected(pool, w, sel)
         out = torch.empty((w.n_requests, w.k), dtype=torch.int32, device="cuda")
         for t in range(w.steps):
@@ -419,6 +423,7 @@ def test_pool_with_each_host_allocation(kind):
     with hs.Pool.for_workload(w, host_alloc=kind) as pool:
         info = pool.info()
         assert info["host_alloc"] == kind
+        assert info["launch_overlap"] == hs.HS_OVERLAP_ON   # a small pool overlaps by default
         assert info["host_bytes"] == w.host_bytes and info["host_mapped_bytes"] >= w.host_bytes
         if kind == hs.HS_HOST_ALLOC_VMM_NUMA and info["device_numa"] >= 0 \
                 and info["host_numa_first"] >= 0:
@@ -450,7 +455,8 @@ def test_host_records_layout():
 
 @pytest.mark.parametrize("cluster", ["1", "4", ""])
 @pytest.mark.parametrize("tight", [False, True])
-def test_back_to_back_resolves_of_one_layer(cluster, tight, monkeypatch):
+@pytest.mark.parametrize("overlap", [hs.HS_OVERLAP_ON, hs.HS_OVERLAP_OFF])
+def test_back_to_back_resolves_of_one_layer(cluster, tight, overlap, monkeypatch):
     """Many resolves of the same pairs enqueued back to back with no host
     synchronisation.  Each launch starts while the previous one still runs
     and decides on metadata that launch is about to change; the decision
@@ -463,7 +469,7 @@ def test_back_to_back_resolves_of_one_layer(cluster, tight, monkeypatch):
                               slots=256 if tight else 512, steps=30, local_window=600)
     sel = traces.generate(w)
     orc = _oracles(w)
-    with hs.Pool.for_workload(w) as pool:
+    with hs.Pool.for_workload(w, launch_overlap=overlap) as pool:
         fill_selected(pool, w, sel)
         dsel = torch.from_numpy(np.ascontiguousarray(sel[:, :, 0])).cuda()   # [T][R][k]
         out = torch.empty((w.steps, w.n_requests, w.k), dtype=torch.int32, device="cuda")

@@ -34,13 +34,17 @@ def _oracle_step(orc: OracleRun, sel_t, pool_ex):
     return dict(pool_ex.map(one, items))
 
 
-def run_and_compare(w, meta_every=1, cache_sample=None, prefetch=False, sel=None):
+def run_and_compare(w, meta_every=1, cache_sample=None, prefetch=False, sel=None,
+                    overlap=hs.HS_OVERLAP_AUTO):
     if sel is None:
         sel = traces.generate(w)
     T, R, NL, k = sel.shape
     orc = OracleRun(w)
     ex = ThreadPoolExecutor(16)
-    with hs.Pool.for_workload(w) as pool:
+    with hs.Pool.for_workload(w, launch_overlap=overlap) as pool:
+        want = overlap if overlap != hs.HS_OVERLAP_AUTO else (
+            hs.HS_OVERLAP_ON if w.host_bytes <= 16 << 30 else hs.HS_OVERLAP_OFF)
+        assert pool.info()["launch_overlap"] == want
         fill_selected(pool, w, sel)
         dsel = device_trace(sel)
         out = torch.empty((NL, R, k), dtype=torch.int32, device="cuda")
@@ -155,9 +159,18 @@ def test_tight_prefetch_full_with_anchor_replay():
 def test_tight_prefetch_small_with_and_without_prefetch():
     w = configs.TIGHT_PREFETCH.with_(n_requests=6, n_positions=20000, k=512, slots=512,
                                      steps=24)
-    run_and_compare(w, meta_every=4, prefetch=False)
-    run_and_compare(w, meta_every=4, prefetch=True)
-    run_and_compare(w, meta_every=4, prefetch="replay")
+    for overlap in (hs.HS_OVERLAP_ON, hs.HS_OVERLAP_OFF):
+        run_and_compare(w, meta_every=4, prefetch=False, overlap=overlap)
+        run_and_compare(w, meta_every=4, prefetch=True, overlap=overlap)
+        run_and_compare(w, meta_every=4, prefetch="replay", overlap=overlap)
+
+
+def test_dsa_mla_small_without_overlap():
+    """Launch overlap off on an 8-request, 8-CTA-cluster shape: the leader
+    fetches the misses of one eighth of each selection."""
+    w = configs.DSA_MLA.with_(n_positions=20000, k=1024, slots=2048, steps=16,
+                              local_window=1500)
+    run_and_compare(w, meta_every=4, overlap=hs.HS_OVERLAP_OFF)
 
 
 @pytest.mark.slow

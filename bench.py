@@ -3,21 +3,28 @@
 A step is one decode step of the whole hot path: every sparse layer's
 resolve (hash build, hit probe, victim choice, host fetch of the misses,
 metadata update, publication) for every request of the batch.  Default
-workload: the DSA/MLA-shaped trace -- 8 requests, 4 sparse layers,
-L_ctx = 131072, k = 2048, B = 4096, 1152-byte records (576 bf16) -- with
-its seeded 256-step selection trace (steps past the end wrap around).
+workload (the headline): the largest one, tight_prefetch -- 64 requests, 8
+sparse layers in two anchor groups, L_ctx = 100352, k = B = 2048,
+1152-byte records (576 bf16), a 59.2 GB pinned host pool -- with its seeded
+128-step selection trace (steps past the end wrap around); then the
+dsa_mla workload (8 requests x 4 layers, B = 4096) beside it (`--also`).
 
-Passes, each on a freshly reset pool (warm-up steps first, then timed ones):
+Passes over the headline, each on a freshly reset pool (warm-up steps
+first, then timed ones):
   graph  -- each step is a CUDA graph of the per-layer hs_resolve launches;
             the L2 is flushed (a 256 MiB write, then a 256 MiB read so
-            that no dirty line is left to write back) before every step and the
-            step itself is timed with CUDA events: ``value``, and, divided
-            by the launches of a step, the resolve kernel's average launch
-            duration inside the graph (``roofline``).
+            that no dirty line is left to write back) before every step and
+            the step itself is timed with CUDA events: ``value``, and,
+            divided by the launches of a step, the resolve kernel's average
+            launch duration inside the graph (``roofline``).
+  prefetch -- the same steps with exact layer-wise prefetch by anchor-plan
+            replay (``prefetch_on``).
+  copy-only -- the same steps' miss records moved by the copy-only kernel
+            alone (``copy_only``; ``roofline.frac_of_copy_only``).
+  measure -- the resolve without its fetch (``no_fetch``: the metadata
+            roofline) and with stage timestamps (``stages``).
   continuous -- blocks of 16 consecutive steps captured as one graph, the
-            L2 flushed before each block only: the per-launch rate of
-            decode steps that follow each other (``continuous``, a
-            diagnostic beside ``value``, which keeps the flush per step).
+            L2 flushed before each block only (``continuous``).
   kernel -- the same steps launched one call at a time with events around
             every launch (``roofline.avg_launch_us_eager``, for context).
   e2e    -- the user's loop through the public API with host buffers: each
@@ -25,7 +32,11 @@ Passes, each on a freshly reset pool (warm-up steps first, then timed ones):
             selections, the resolves and the device -> host copy of the
             published slots, replayed and synchronised, all inside the timed
             region (``e2e``).
-The host-link ceiling is measured in the same run (pinned H2D memcpy and a
+The headline's pool is allocated first: on the GB300 machines measured, host
+reads of pinned pools allocated after other large pinned pools had been
+freed ran slower and sped up again over seconds, so the other workloads
+are timed after it, in the same process (``other_workloads``).  The
+host-link ceiling is measured in the same run (pinned H2D memcpy and a
 scattered-record GPU-load probe, best of 10).  The CPU oracle is timed on
 the host's cores over a stated sample (``cpu_baseline``).
 
@@ -374,10 +385,10 @@ def run_gpu(args, w, rank, world, dist_on, lite=False):
     R, NL, k, B, W, T = w.n_requests, w.n_layers, w.k, w.slots, w.record_bytes, w.steps
 
     kind = HOST_ALLOC[args.host_alloc]
-    h2d_gbs, gather_gbs = hs.hs_link_probe(1 << 30, 10, W, kind)
-
     sel = traces.generate(w)
     dsel = torch.from_numpy(np.ascontiguousarray(sel.transpose(0, 2, 1, 3))).to(dev)
+    # the pool first: a process's first large pinned allocation is the one
+    # the host's memory serves best (see host_pages and the docstring)
     t_fill = time.perf_counter()
     pool = hs.Pool.for_workload(w, host_alloc=kind, launch_overlap=OVERLAP[args.launch_overlap])
     pool_info = pool.info()
@@ -385,7 +396,12 @@ def run_gpu(args, w, rank, world, dist_on, lite=False):
         for l in range(NL):
             records.fill(pool.host_records(r, l).ctypes.data, w, r, l)
     pool_info["create_and_fill_s"] = time.perf_counter() - t_fill
-    pool_info["pages"] = host_pages(pool.host_records(0, 0).ctypes.data, w.host_bytes)
+    h2d_gbs, gather_gbs = hs.hs_link_probe(1 << 30, 10, W, kind)
+    base_addr = pool.host_records(0, 0).ctypes.data
+    pool_info["pages"] = host_pages(base_addr, w.host_bytes)
+    pool_info["host_address"] = hex(base_addr)
+    pool_info["host_address_mod_2mib"] = base_addr % (2 << 20)
+    pool_info["host_address_mod_512mib"] = base_addr % (512 << 20)
     out = torch.empty((NL, R, k), dtype=torch.int32, device=dev)
     flush = L2Flush(dev)
     main = torch.cuda.current_stream()
@@ -1527,15 +1543,16 @@ def main(argv=None):
             run = run_prefetch_overlap if args.prefetch_overlap else run_attention
             print(json.dumps(run(args, w)))
         return 0
-    # the smaller workloads first: their pools are allocated before the
-    # headline's large one has been pinned and freed
-    others = {}
-    for name in also:
-        lite = run_gpu(args, rank_workload(shaped(name), rank), rank, world, dist_on, lite=True)
-        others[name] = lite
+    # the headline first: its pool is the process's first large pinned
+    # allocation; the other workloads follow
     res = run_gpu(args, w, rank, world, dist_on)
     res["config"]["host_numa_node"] = numa
     res["config"]["process_cpus"] = numa_cpus
+    others = {}
+    for name in also:
+        lite = run_gpu(args, rank_workload(shaped(name), rank), rank, world, dist_on, lite=True)
+        lite["timed_after"] = "the headline workload, in the same process"
+        others[name] = lite
     if others:
         res["other_workloads"] = others
     if rank == 0:

@@ -63,7 +63,7 @@ if ROOT not in sys.path:
 METRIC = ("resolves/sec and miss-fetch GB/s (fraction of measured pinned H2D BW) "
           "at 1 GB300")
 L2_FLUSH_BYTES = 256 << 20
-HOST_ALLOC = {"auto": 0, "pinned": 1, "vmm": 2}
+HOST_ALLOC = {"auto": 0, "pinned": 1, "vmm": 2, "thp": 3}
 OVERLAP = {"auto": 0, "on": 1, "off": 2}
 CONT_STEPS, CONT_BLOCKS = 16, 3
 
@@ -101,6 +101,22 @@ class L2Flush:
     def __call__(self, i):
         self.w.fill_(i)
         self.sink = self.r.max()
+
+
+class nvtx:
+    """An NVTX range around a bench pass (seen by ncu --nvtx and nsys)."""
+
+    def __init__(self, name: str):
+        self.name = name
+
+    def __enter__(self):
+        import torch
+        torch.cuda.nvtx.range_push(self.name)
+        return self
+
+    def __exit__(self, *exc):
+        import torch
+        torch.cuda.nvtx.range_pop()
 
 
 def workload_name(w) -> str:
@@ -448,11 +464,13 @@ def run_gpu(args, w, rank, world, dist_on, lite=False):
     barrier()
     sampler.start()
     wall0 = time.perf_counter()
+    torch.cuda.nvtx.range_push("timed steps")
     for i in range(K):
         flush(i)
         ev[i][0].record(main)
         graphs[(Wm + i) % T].replay()
         ev[i][1].record(main)
+    torch.cuda.nvtx.range_pop()
     barrier()
     wall_graph = time.perf_counter() - wall0
     sampler.stop()
@@ -497,8 +515,10 @@ def run_gpu(args, w, rank, world, dist_on, lite=False):
 
     # ---- exact prefetch in the pure resolve step, and the copy-only rate of
     # the same miss records (both beside `value`) ----------------------------
-    prefetch_on = run_prefetch_pass(pool, w, dsel, flush, main, cap, K, Wm, h2d_gbs)
-    copy_only = run_copy_only(pool, w, dsel, flush, main, cap, K, Wm, h2d_gbs)
+    with nvtx("prefetch pass"):
+        prefetch_on = run_prefetch_pass(pool, w, dsel, flush, main, cap, K, Wm, h2d_gbs)
+    with nvtx("copy-only pass"):
+        copy_only = run_copy_only(pool, w, dsel, flush, main, cap, K, Wm, h2d_gbs)
 
     # ---- continuous pass (diagnostic, not `value`) --------------------------
     # blocks of CONT_STEPS consecutive steps captured as one graph, L2
@@ -541,7 +561,8 @@ def run_gpu(args, w, rank, world, dist_on, lite=False):
     }
 
     # ---- measurement passes: no fetch, stage stamps (diagnostics) ------------
-    measure = run_measure_passes(pool, w, dsel, flush, main, cap, K, Wm)
+    with nvtx("measurement passes"):
+        measure = run_measure_passes(pool, w, dsel, flush, main, cap, K, Wm)
 
     # ---- kernel pass (per-launch events, eager launches) ---------------------
     pool.reset()
@@ -1018,7 +1039,8 @@ def run_prefetch_overlap(args, w):
     R, NL, k, T = w.n_requests, w.n_layers, w.k, w.steps
     sel = traces.generate(w)
     dsel = torch.from_numpy(np.ascontiguousarray(sel.transpose(0, 2, 1, 3))).to(dev)
-    pool = hs.Pool.for_workload(w)
+    pool = hs.Pool.for_workload(w, host_alloc=HOST_ALLOC[args.host_alloc],
+                                launch_overlap=OVERLAP[args.launch_overlap])
     for r in range(R):
         for l in range(NL):
             records.fill(pool.host_records(r, l).ctypes.data, w, r, l)
@@ -1131,6 +1153,7 @@ def run_prefetch_overlap(args, w):
     attn_res = time_attention(lambda: attention(0), flush, main, R, k, heads,
                               args.steps) if attn else None
     kern = time_prefetch_kernels(pool, w, dsel, out, plans, flush, main, args, replay)
+    pool_launch_overlap = pool.info()["launch_overlap"]
     pool.close()
     alone = results["resolve"]
     hidden_off = 1.0 - (results["off"] - results["compute"]) / alone
@@ -1143,6 +1166,7 @@ def run_prefetch_overlap(args, w):
                          (results["off"] - results["compute"]),
         "higher_is_better": True,
         "config": {"workload": workload_name(w), "shared_layers_per_step": len(shared),
+                   "launch_overlap": "on" if pool_launch_overlap == hs.HS_OVERLAP_ON else "off",
                    "prefetch_source": ("the anchor's miss plan written by its resolve "
                                        "(hs_resolve_anchor)" if replay else
                                        "hs_prefetch_plan per shared layer"),
@@ -1365,7 +1389,7 @@ def link_sweep(sizes_gib, record_bytes: int) -> dict:
     from hierarchical_kv_cache_resolve_gb300 import hs
     rows = []
     for gib in sizes_gib:
-        for name in ("pinned", "vmm"):
+        for name in ("pinned", "vmm", "thp"):
             t0 = time.perf_counter()
             try:
                 h2d, gather = hs.hs_link_probe(gib << 30, 3, record_bytes, HOST_ALLOC[name])

@@ -127,7 +127,7 @@ int hs_create_pool(const hs_pool_desc *desc, hs_pool **out) {
     if (d.n_requests < 1 || d.n_layers < 1 || d.n_positions < 1 ||
         d.n_positions > INT32_MAX || d.record_bytes < 16 || d.record_bytes % 16 != 0 ||
         d.slots < 1 || d.slots > 32767 || d.max_k < 1 || d.max_k > d.slots ||
-        d.host_alloc < HS_HOST_ALLOC_AUTO || d.host_alloc > HS_HOST_ALLOC_VMM_NUMA ||
+        d.host_alloc < HS_HOST_ALLOC_AUTO || d.host_alloc > HS_HOST_ALLOC_THP_REGISTERED ||
         d.launch_overlap < HS_OVERLAP_AUTO || d.launch_overlap > HS_OVERLAP_OFF)
         return HS_ERR_INVALID_ARG;
     // index arithmetic limits of the kernels (32-bit chunk counters and
@@ -417,7 +417,7 @@ int hs_attention_status(uint32_t *status) {
 int hs_link_probe(size_t bytes, int32_t reps, int32_t record_bytes, int32_t host_alloc,
                   double *h2d_gbs, double *gather_gbs) {
     if (bytes < (size_t)record_bytes || reps < 1 || record_bytes < 16 || record_bytes % 16 ||
-        host_alloc < HS_HOST_ALLOC_AUTO || host_alloc > HS_HOST_ALLOC_VMM_NUMA)
+        host_alloc < HS_HOST_ALLOC_AUTO || host_alloc > HS_HOST_ALLOC_THP_REGISTERED)
         return HS_ERR_INVALID_ARG;
     const int64_t n_rec = (int64_t)(bytes / (size_t)record_bytes);
     if (n_rec > INT32_MAX) return HS_ERR_INVALID_ARG;

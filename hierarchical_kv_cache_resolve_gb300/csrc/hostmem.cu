@@ -3,7 +3,7 @@
 // HiSparse", section 2 "Two-Level Hierarchy": every KV record lives in
 // pinned, device-mapped host memory).
 //
-// Two ways to provide it:
+// Three ways to provide it:
 //   HS_HOST_ALLOC_PINNED   cudaHostAlloc(Mapped | Portable), allocated
 //                          while the calling thread prefers the host NUMA
 //                          node the device reports as its closest
@@ -14,16 +14,23 @@
 //                          device reports as its closest
 //                          (cudaDevAttrHostNumaId), mapped at one virtual
 //                          address range that both the device and the host
-//                          may read and write.
+//                          may read and write;
+//   HS_HOST_ALLOC_THP_REGISTERED anonymous memory in transparent huge pages,
+//                          first touched on that node, pinned and mapped
+//                          with cudaHostRegister.
 // The driver API entry points are looked up through the runtime
 // (cudaGetDriverEntryPointByVersion), so the library does not link
 // libcuda itself.
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <thread>
+#include <vector>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <sys/mman.h>
 #include <sys/syscall.h>
 #include <unistd.h>
 
@@ -157,7 +164,12 @@ class PreferNode {
     }
     ~PreferNode() {
 #if defined(SYS_set_mempolicy)
-        if (active_) syscall(SYS_set_mempolicy, old_mode_, old_mask_, (unsigned long)kBits + 1);
+        if (!active_) return;
+        // the default policy takes no node mask
+        if ((old_mode_ & 0xFF) == 0)
+            syscall(SYS_set_mempolicy, old_mode_, nullptr, 0UL);
+        else
+            syscall(SYS_set_mempolicy, old_mode_, old_mask_, (unsigned long)kBits + 1);
 #endif
     }
 
@@ -167,6 +179,19 @@ class PreferNode {
     unsigned long old_mask_[kWords] = {};
     bool active_ = false;
 };
+
+// Transparent-huge-page size of the kernel (PMD size), 2 MiB if unknown.
+size_t thp_size() {
+    size_t v = 0;
+    if (FILE *f = std::fopen("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size", "r")) {
+        unsigned long long x = 0;
+        if (std::fscanf(f, "%llu", &x) == 1) v = (size_t)x;
+        std::fclose(f);
+    }
+    return v >= 4096 ? v : ((size_t)2 << 20);
+}
+
+int alloc_thp_registered(size_t bytes, int dev, HostBuffer *out);
 
 }  // namespace
 
@@ -179,10 +204,64 @@ int device_host_numa(int dev) {
     return numa;
 }
 
+namespace {
+
+// Anonymous memory in transparent huge pages (madvise on the mapping only),
+// aligned to the huge-page size, first touched by threads preferring the
+// device's NUMA node, then pinned and mapped for the device with
+// cudaHostRegister.
+int alloc_thp_registered(size_t bytes, int dev, HostBuffer *out) {
+    const size_t hp = thp_size();
+    const size_t size = (bytes + hp - 1) / hp * hp;
+    void *raw = mmap(nullptr, size + hp, PROT_READ | PROT_WRITE,
+                     MAP_PRIVATE | MAP_ANONYMOUS | MAP_NORESERVE, -1, 0);
+    if (raw == MAP_FAILED) return HS_ERR_NOMEM;
+    uint8_t *p = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(raw) + hp - 1) / hp * hp);
+    madvise(p, size, MADV_HUGEPAGE);
+    const int numa = device_host_numa(dev);
+    // first touch in parallel, one huge page at a time
+    const size_t pages = size / hp;
+    unsigned nt = std::thread::hardware_concurrency();
+    if (nt < 1) nt = 1;
+    if (nt > 64) nt = 64;
+    if ((size_t)nt > pages) nt = (unsigned)pages;
+    std::vector<std::thread> th;
+    for (unsigned t = 0; t < nt; ++t)
+        th.emplace_back([=] {
+            PreferNode prefer(numa);
+            for (size_t i = t; i < pages; i += nt) std::memset(p + i * hp, 0, hp);
+        });
+    for (auto &x : th) x.join();
+    if (cudaHostRegister(p, size, cudaHostRegisterMapped | cudaHostRegisterPortable) != cudaSuccess) {
+        cudaGetLastError();
+        munmap(raw, size + hp);
+        return HS_ERR_NOMEM;
+    }
+    void *d = nullptr;
+    if (cudaHostGetDevicePointer(&d, p, 0) != cudaSuccess) {
+        cudaHostUnregister(p);
+        munmap(raw, size + hp);
+        return HS_ERR_CUDA;
+    }
+    out->host = p;
+    out->dev = d;
+    out->bytes = bytes;
+    out->mapped = size;
+    out->granularity = hp;
+    out->handle = reinterpret_cast<unsigned long long>(raw);
+    out->kind = HS_HOST_ALLOC_THP_REGISTERED;
+    out->numa = numa;
+    return HS_OK;
+}
+
+}  // namespace
+
 int host_alloc(size_t bytes, int kind, int dev, HostBuffer *out) {
     std::memset(out, 0, sizeof(*out));
     out->numa = -1;
     if (kind == HS_HOST_ALLOC_VMM_NUMA) return alloc_vmm(bytes, dev, out);
+    if (kind == HS_HOST_ALLOC_THP_REGISTERED) return alloc_thp_registered(bytes, dev, out);
     if (kind != HS_HOST_ALLOC_PINNED) return HS_ERR_INVALID_ARG;
     void *h = nullptr, *d = nullptr;
     const int numa = device_host_numa(dev);
@@ -216,6 +295,9 @@ void host_free(HostBuffer *b) {
         v.unmap(va, b->mapped);
         v.release((CUmemGenericAllocationHandle)b->handle);
         v.address_free(va, b->mapped);
+    } else if (b->kind == HS_HOST_ALLOC_THP_REGISTERED) {
+        cudaHostUnregister(b->host);
+        munmap(reinterpret_cast<void *>(b->handle), b->mapped + b->granularity);
     } else {
         cudaFreeHost(b->host);
     }

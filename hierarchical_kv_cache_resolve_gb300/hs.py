@@ -28,6 +28,7 @@ HS_ERR_UNSUPPORTED = -6
 HS_HOST_ALLOC_AUTO = 0
 HS_HOST_ALLOC_PINNED = 1
 HS_HOST_ALLOC_VMM_NUMA = 2
+HS_HOST_ALLOC_THP_REGISTERED = 3
 
 HS_OVERLAP_AUTO = 0
 HS_OVERLAP_ON = 1

@@ -129,6 +129,14 @@ typedef struct {
  * aligned virtual range readable and writable by the device and the host
  * at the same address. */
 #define HS_HOST_ALLOC_VMM_NUMA 2
+/* Anonymous host memory in transparent huge pages (madvise on the mapping,
+ * aligned to the huge-page size), first touched by threads preferring the
+ * device's host NUMA node, then pinned and mapped for the device with
+ * cudaHostRegister(Mapped | Portable).  Measured on GB300 with a 59 GB pool
+ * in 512 MiB pages: scattered reads past the translation reach about twice
+ * as fast as cudaHostAlloc memory once warm, but the first resolves over a
+ * new pool run far slower (seconds), so it is not the default. */
+#define HS_HOST_ALLOC_THP_REGISTERED 3
 
 typedef struct {
     uint64_t resolves;          /* resolves committed (one per request per call) */

@@ -54,7 +54,7 @@ def _desc(**kw):
 @pytest.mark.parametrize("bad", [
     dict(n_requests=0), dict(n_layers=0), dict(n_positions=0), dict(n_positions=1 << 31),
     dict(record_bytes=100), dict(record_bytes=0), dict(slots=0), dict(slots=40000),
-    dict(max_k=0), dict(max_k=65), dict(host_alloc=-1), dict(host_alloc=3),
+    dict(max_k=0), dict(max_k=65), dict(host_alloc=-1), dict(host_alloc=4),
     dict(launch_overlap=-1), dict(launch_overlap=3)])
 def test_create_pool_rejects_bad_descriptors(lib, bad):
     h = ctypes.c_void_p(1234)

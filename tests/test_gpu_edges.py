@@ -407,20 +407,42 @@ def test_pools_of_different_sizes_coexist():
                 assert np.array_equal(gs[r], orc_s[(r, 0)].resolve(sel_s[t, r, 0], out_base=r * small.slots)[1])
 
 
-@pytest.mark.parametrize("kind", [hs.HS_HOST_ALLOC_PINNED, hs.HS_HOST_ALLOC_VMM_NUMA])
+@pytest.mark.parametrize("kind", [hs.HS_HOST_ALLOC_PINNED, hs.HS_HOST_ALLOC_VMM_NUMA,
+                                  hs.HS_HOST_ALLOC_THP_REGISTERED])
 def test_link_probe_reports_bandwidth(kind):
     h2d, gather = hs.hs_link_probe(256 << 20, reps=3, record_bytes=1152, host_alloc=kind)
     assert h2d > 1.0 and gather > 1.0
 
 
-@pytest.mark.parametrize("kind", [hs.HS_HOST_ALLOC_PINNED, hs.HS_HOST_ALLOC_VMM_NUMA])
+def _thread_mempolicy():
+    """The calling thread's NUMA policy mode (get_mempolicy), None where
+    the syscall is unknown."""
+    import ctypes
+    import os
+    nr = {"aarch64": 236, "x86_64": 239}.get(os.uname().machine)
+    if nr is None:
+        return None
+    mode = ctypes.c_int(-1)
+    mask = (ctypes.c_ulong * 16)()
+    libc = ctypes.CDLL(None, use_errno=True)
+    if libc.syscall(ctypes.c_long(nr), ctypes.byref(mode), mask, ctypes.c_ulong(1025),
+                    None, ctypes.c_ulong(0)) != 0:
+        return None
+    return mode.value, tuple(mask)
+
+
+@pytest.mark.parametrize("kind", [hs.HS_HOST_ALLOC_PINNED, hs.HS_HOST_ALLOC_VMM_NUMA,
+                                  hs.HS_HOST_ALLOC_THP_REGISTERED])
 def test_pool_with_each_host_allocation(kind):
     """Both host allocations hold the records the kernels fetch: the same
     trace gives the oracle's slots and slot contents either way."""
     w = configs.TINY.with_(n_requests=3, n_layers=2, steps=12)
     sel = traces.generate(w)
     orc = _oracles(w)
+    policy = _thread_mempolicy()
     with hs.Pool.for_workload(w, host_alloc=kind) as pool:
+        # the pool is placed on the device's node; the caller's policy is back
+        assert _thread_mempolicy() == policy
         info = pool.info()
         assert info["host_alloc"] == kind
         assert info["launch_overlap"] == hs.HS_OVERLAP_ON   # a small pool overlaps by default

@@ -216,6 +216,52 @@ def test_dsa_mla_full_as_the_benchmark_runs_it():
     ex.shutdown()
 
 
+@pytest.mark.slow
+def test_tight_prefetch_full_as_the_benchmark_runs_it():
+    """The headline's own launch configuration at full size (64 requests x
+    8 layers, 59.2 GB pool, launch overlap off by the pool policy, the
+    leader fetching its share): one CUDA graph of the eight layers' resolves
+    per step, replayed step after step with no host synchronisation and the
+    L2 flushed between steps; every step's published slots, then the final
+    metadata and sampled slot contents, against the oracle."""
+    w = configs.TIGHT_PREFETCH
+    T = 12
+    sel = traces.generate(w)[:T]
+    R, NL, k = w.n_requests, w.n_layers, w.k
+    orc = OracleRun(w)
+    ex = ThreadPoolExecutor(16)
+    with hs.Pool.for_workload(w) as pool:
+        assert pool.info()["launch_overlap"] == hs.HS_OVERLAP_OFF
+        fill_selected(pool, w, sel)
+        dsel = device_trace(sel)
+        out = torch.empty((T, NL, R, k), dtype=torch.int32, device="cuda")
+        flush = torch.empty(64 << 20, dtype=torch.int32, device="cuda")
+        cap = torch.cuda.Stream()
+        graphs = []
+        for t in range(T):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                for l in range(NL):
+                    hs.hs_resolve(pool.handle, l, R, None, dsel[t, l], k, out[t, l], None, cap)
+            graphs.append(g)
+        torch.cuda.synchronize()
+        for t in range(T):
+            flush.fill_(t)
+            graphs[t].replay()
+        got = out.cpu().numpy()
+        for t in range(T):
+            ores = _oracle_step(orc, sel[t], ex)
+            for (r, l), (o, m) in ores.items():
+                assert np.array_equal(got[t, l, r], o), (t, r, l)
+        for (r, l), p in orc.state.items():
+            check_metadata(pool, w, l, r, p, T)
+            check_cache(pool, w, l, r, p.slot_pos, sample=64)
+        st = pool.stats()
+        assert st["status"] == 0 and st["resolves"] == T * R * NL
+        assert st["fetched_bytes"] == sum(p.fetched_bytes for p in orc.state.values())
+    ex.shutdown()
+
+
 @pytest.mark.parametrize("source", ["plan", "replay"])
 def test_tight_prefetch_scheduled_like_the_overlap_benchmark(source):
     """Exact prefetch in the schedule of the overlap benchmark: at each

@@ -67,16 +67,20 @@ HOST_ALLOC = {"auto": 0, "pinned": 1, "vmm": 2, "thp": 3}
 OVERLAP = {"auto": 0, "on": 1, "off": 2}
 CONT_STEPS, CONT_BLOCKS = 16, 3
 
-# Counters of one steady-state resolve launch from an ncu capture (dsa_mla
-# shape, L_ctx cut to 16384: same batch, k, B, W), valid only for the kernel
-# sources they were taken on: reported as null once those sources change.
-PROFILED_SOURCES = {"resolve.cu": "5969faa6566a9b98", "hs_internal.cuh": "a609866f73457959"}
-PROFILED_LAUNCH = {"dram_bytes": 875_008, "link_bytes": 2_073_600,
-                   "algorithmic_link_bytes": 2_073_600}
+# Counters of one steady-state resolve launch from an ncu capture
+# (profiles/resolve_kernel_tight_prefetch_full.md: tight_prefetch at full
+# size, one layer of 64 resolves), valid only for that workload and for the
+# kernel sources they were taken on: reported as null otherwise.
+PROFILED_WORKLOAD = "tight_prefetch"
+PROFILED_SOURCES = {"resolve.cu": "a289626c2cdcb788", "hs_internal.cuh": "0f2f48f99de540e7"}
+PROFILED_LAUNCH = {"dram_bytes": 8_615_680 + 73_216, "link_bytes": 22_639_104,
+                   "algorithmic_link_bytes": 22_634_496}
 
 
-def profiled_counters():
+def profiled_counters(workload_name: str):
     import hashlib
+    if workload_name != PROFILED_WORKLOAD:
+        return None
     csrc = os.path.join(ROOT, "hierarchical_kv_cache_resolve_gb300", "csrc")
     for name, digest in PROFILED_SOURCES.items():
         with open(os.path.join(csrc, name), "rb") as f:
@@ -617,7 +621,7 @@ def run_gpu(args, w, rank, world, dist_on, lite=False):
     pool.close()
 
     peaks = load_peaks()
-    prof = profiled_counters()
+    prof = profiled_counters(w.name)
     hbm_peak = peaks.get("hbm_gbs") if peaks else None
     miss_gbs = total_fetched / dev_s_max / 1e9
     link_achieved = link_bytes_per_launch / avg_launch_s / 1e9

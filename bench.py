@@ -417,6 +417,10 @@ def run_gpu(args, w, rank, world, dist_on, lite=False):
             records.fill(pool.host_records(r, l).ctypes.data, w, r, l)
     pool_info["create_and_fill_s"] = time.perf_counter() - t_fill
     h2d_gbs, gather_gbs = hs.hs_link_probe(1 << 30, 10, W, kind)
+    # the records are written: read them once from the device and resolve
+    # synthetic steps, then reset (hs_warm_pool; outside every timed region)
+    pool.warm()
+    pool_info["warmup_us"] = pool.info()["warmup_us"]
     base_addr = pool.host_records(0, 0).ctypes.data
     pool_info["pages"] = host_pages(base_addr, w.host_bytes)
     pool_info["host_address"] = hex(base_addr)
@@ -608,6 +612,15 @@ def run_gpu(args, w, rank, world, dist_on, lite=False):
     def e2e_step(t):
         e2e_graphs[t].replay()
         main.synchronize()
+
+    # every step's selections, written by the CPU into one pinned buffer, are
+    # read once from the device before timing (the device's first read of
+    # host memory the CPU has written is slow on these machines; a serving
+    # loop reuses its pinned buffers), and the output buffer written once
+    for t in range(T):
+        stage.copy_(host_sel[t], non_blocking=True)
+    host_out.copy_(out, non_blocking=True)
+    main.synchronize()
 
     for s in range(Wm):
         e2e_step(s % T)
@@ -1048,6 +1061,7 @@ def run_prefetch_overlap(args, w):
     for r in range(R):
         for l in range(NL):
             records.fill(pool.host_records(r, l).ctypes.data, w, r, l)
+    pool.warm()
     # published slots; before the first resolve, k distinct rows per request
     B = w.slots
     out = (torch.arange(R, dtype=torch.int32, device=dev)[:, None] * B

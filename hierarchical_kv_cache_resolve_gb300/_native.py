@@ -108,7 +108,8 @@ class PoolInfo(ctypes.Structure):
                 ("device_numa", ctypes.c_int32), ("host_numa_first", ctypes.c_int32),
                 ("host_numa_last", ctypes.c_int32), ("launch_overlap", ctypes.c_int32),
                 ("host_bytes", ctypes.c_uint64), ("host_mapped_bytes", ctypes.c_uint64),
-                ("host_granularity", ctypes.c_uint64), ("device_bytes", ctypes.c_uint64)]
+                ("host_granularity", ctypes.c_uint64), ("device_bytes", ctypes.c_uint64),
+                ("host_huge_bytes", ctypes.c_uint64), ("warmup_us", ctypes.c_uint64)]
 
 
 class Stats(ctypes.Structure):
@@ -134,7 +135,7 @@ class LayerState(ctypes.Structure):
 
 
 EXPORTS = ("hs_create_pool", "hs_destroy_pool", "hs_host_records", "hs_device_views",
-           "hs_pool_info", "hs_device_host_numa",
+           "hs_pool_info", "hs_device_host_numa", "hs_touch_records", "hs_warm_pool",
            "hs_resolve", "hs_resolve_anchor", "hs_resolve_measure", "hs_measure_stamp_slots", "hs_plan_bytes",
            "hs_prefetch_plan", "hs_prefetch_copy",
            "hs_stats", "hs_reset", "hs_link_probe", "hs_kernels_per_call", "hs_strerror",
@@ -152,6 +153,8 @@ def _declare(lib):
         "hs_device_views": ([P, i32, ctypes.POINTER(Views)], ctypes.c_int),
         "hs_pool_info": ([P, ctypes.POINTER(PoolInfo)], ctypes.c_int),
         "hs_device_host_numa": ([i32], ctypes.c_int),
+        "hs_touch_records": ([P, i32, i32, vp], ctypes.c_int),
+        "hs_warm_pool": ([P], ctypes.c_int),
         "hs_resolve": ([P, i32, i32, vp, vp, i32, vp, vp, vp], ctypes.c_int),
         "hs_resolve_anchor": ([P, i32, i32, vp, vp, i32, vp, vp, vp], ctypes.c_int),
         "hs_resolve_measure": ([P, i32, i32, vp, vp, i32, vp, i32, vp, vp], ctypes.c_int),

@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in include/hs.h: pool allocation,
 // argument checks, launches, counters and the link probe.
 #include <algorithm>
+#include <chrono>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -18,6 +19,7 @@ struct hs_pool {
     int sm_count = 0;
     int cluster_override = 0;
     bool overlap = true;  // consecutive resolves may overlap (launch_overlap)
+    double warmup_us = 0;  // the huge-page pool's warm-up at creation
     hs::HostBuffer host = {};
     size_t host_bytes = 0;
     hs::DevPool dp = {};
@@ -41,7 +43,8 @@ void free_device(hs_pool *p) {
     hs::host_free(&p->host);
 }
 
-// The host allocation a pool or probe uses for HS_HOST_ALLOC_AUTO.
+// The host allocation a probe uses for HS_HOST_ALLOC_AUTO (a pool picks
+// by its size, see hs_create_pool).
 int auto_host_alloc() { return HS_HOST_ALLOC_PINNED; }
 
 int reset_state(hs_pool *p) {
@@ -58,6 +61,51 @@ int reset_state(hs_pool *p) {
         !cuda_ok(cudaDeviceSynchronize()))
         return HS_ERR_CUDA;
     return HS_OK;
+}
+
+int pick_cluster(const hs_pool *p, int n_req);
+int lead_share(const hs_pool *p, int k, int cluster);
+
+// Synthetic resolves over every (request, layer) pair, then the empty
+// state again (hs_warm_pool): kWarmSteps steps, each a new set of k
+// distinct positions per request, so that every selection misses and every
+// slot is written.
+constexpr int kWarmSteps = 16;
+int warm_pool(hs_pool *p) {
+    const int R = p->desc.n_requests, NL = p->desc.n_layers;
+    const int64_t L = p->desc.n_positions;
+    const int k = (int)std::min<int64_t>(p->desc.max_k, L);
+    const int64_t G = std::max<int64_t>(1, L / k), D = std::max<int64_t>(1, G / 7);
+    std::vector<int32_t> sel((size_t)R * k);
+    int32_t *dsel = nullptr, *dout = nullptr;
+    int rc = HS_OK;
+    if (!cuda_ok(cudaMalloc(&dsel, sel.size() * 4)) || !cuda_ok(cudaMalloc(&dout, sel.size() * 4))) {
+        rc = HS_ERR_NOMEM;
+    } else {
+        const int cluster = pick_cluster(p, R);
+        for (int step = 0; step < kWarmSteps && rc == HS_OK; ++step) {
+            // positions (base_r + step * D + i * G) mod L: distinct, since k * G <= L
+            for (int r = 0; r < R; ++r) {
+                const int64_t base = ((int64_t)r * 7919) % L;
+                for (int i = 0; i < k; ++i)
+                    sel[(size_t)r * k + i] = (int32_t)((base + step * D + (int64_t)i * G) % L);
+            }
+            if (!cuda_ok(cudaMemcpy(dsel, sel.data(), sel.size() * 4, cudaMemcpyHostToDevice))) {
+                rc = HS_ERR_CUDA;
+                break;
+            }
+            for (int l = 0; l < NL && rc == HS_OK; ++l)
+                if (!cuda_ok(hs::launch_resolve(p->dp, l, R, nullptr, dsel, k, dout, nullptr, cluster,
+                                                0, p->anchor[l], nullptr, p->overlap,
+                                                lead_share(p, k, cluster))))
+                    rc = HS_ERR_CUDA;
+        }
+        if (rc == HS_OK && !cuda_ok(cudaDeviceSynchronize())) rc = HS_ERR_CUDA;
+    }
+    cudaFree(dsel);
+    cudaFree(dout);
+    if (rc != HS_OK) return rc;
+    return reset_state(p);
 }
 
 // Cluster size for a resolve over n_req requests: the largest power of two
@@ -176,8 +224,19 @@ int hs_create_pool(const hs_pool_desc *desc, hs_pool **out) {
     p->pt_bytes = pairs * (size_t)d.n_positions * 4;
     p->host_bytes = host_bytes;
 
-    int rc = hs::host_alloc(host_bytes, d.host_alloc ? d.host_alloc : auto_host_alloc(), dev,
-                            &p->host);
+    int rc = HS_OK;
+    if (d.host_alloc != HS_HOST_ALLOC_AUTO) {
+        rc = hs::host_alloc(host_bytes, d.host_alloc, dev, &p->host);
+    } else if (host_bytes > HS_OVERLAP_AUTO_MAX_HOST_BYTES) {
+        // past the translation reach: huge pages if the kernel backs (nearly)
+        // the whole pool with them, cudaHostAlloc otherwise
+        rc = hs::host_alloc(host_bytes, HS_HOST_ALLOC_THP_REGISTERED, dev, &p->host);
+        if (rc == HS_OK && p->host.huge_bytes < p->host.mapped / 10 * 9) hs::host_free(&p->host);
+        if (rc != HS_OK || !p->host.host)
+            rc = hs::host_alloc(host_bytes, HS_HOST_ALLOC_PINNED, dev, &p->host);
+    } else {
+        rc = hs::host_alloc(host_bytes, HS_HOST_ALLOC_PINNED, dev, &p->host);
+    }
     if (rc != HS_OK) goto fail;
     p->desc.host_alloc = p->host.kind;
     p->dp.host = static_cast<const uint8_t *>(p->host.dev);
@@ -229,6 +288,41 @@ int hs_host_records(hs_pool *pool, int32_t req, int32_t layer, void **host_ptr) 
     return HS_OK;
 }
 
+int hs_touch_records(hs_pool *pool, int32_t req, int32_t layer, void *stream) {
+    if (!pool || req < -1 || req >= pool->desc.n_requests || layer < -1 ||
+        layer >= pool->desc.n_layers)
+        return HS_ERR_INVALID_ARG;
+    const size_t per = (size_t)pool->desc.n_positions * pool->desc.record_bytes;
+    const int NL = pool->desc.n_layers;
+    const uint8_t *base = static_cast<const uint8_t *>(pool->host.dev);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // host[r][l][L][W]: all of a request's layers, or all requests, are
+    // contiguous; one (request, layer) region otherwise
+    cudaError_t e = cudaSuccess;
+    if (req < 0 && layer < 0) {
+        e = hs::launch_touch(base, pool->host_bytes, pool->sm_count, st);
+    } else if (layer < 0) {
+        e = hs::launch_touch(base + (size_t)req * NL * per, (size_t)NL * per, pool->sm_count, st);
+    } else {
+        for (int r = (req < 0 ? 0 : req); r < (req < 0 ? pool->desc.n_requests : req + 1) &&
+                                           e == cudaSuccess; ++r)
+            e = hs::launch_touch(base + ((size_t)r * NL + layer) * per, per, pool->sm_count, st);
+    }
+    return cuda_ok(e) ? HS_OK : HS_ERR_CUDA;
+}
+
+int hs_warm_pool(hs_pool *pool) {
+    if (!pool) return HS_ERR_INVALID_ARG;
+    const auto t0 = std::chrono::steady_clock::now();
+    int rc = hs_touch_records(pool, -1, -1, nullptr);
+    if (rc == HS_OK && !cuda_ok(cudaDeviceSynchronize())) rc = HS_ERR_CUDA;
+    if (rc == HS_OK) rc = warm_pool(pool);
+    if (rc == HS_OK)
+        pool->warmup_us =
+            std::chrono::duration<double, std::micro>(std::chrono::steady_clock::now() - t0).count();
+    return rc;
+}
+
 int hs_device_host_numa(int32_t device) {
     int n = 0;
     if (cudaGetDeviceCount(&n) != cudaSuccess) {
@@ -252,6 +346,8 @@ int hs_pool_info(hs_pool *pool, hs_pool_info_t *out) {
     out->host_bytes = pool->host_bytes;
     out->host_mapped_bytes = pool->host.mapped;
     out->host_granularity = pool->host.granularity;
+    out->host_huge_bytes = pool->host.huge_bytes;
+    out->warmup_us = (uint64_t)pool->warmup_us;
     const size_t pairs = pool->meta_pairs, B = (size_t)pool->desc.slots;
     out->device_bytes = pool->cache_bytes + pool->pt_bytes + pairs * B * (4 + 4 + 2) + pairs * 8 +
                         (size_t)pool->desc.n_layers * hs::CTR_COUNT * 8 + 4;

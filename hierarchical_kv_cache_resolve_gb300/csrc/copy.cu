@@ -89,6 +89,17 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
+// One 4-byte device read of every 256 bytes of [p, p + bytes) (volatile
+// asm: kept although the values are unused).
+__global__ void touch_kernel(const uint8_t *__restrict__ p, size_t bytes) {
+    const size_t n = bytes / 256;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+         i += (size_t)gridDim.x * blockDim.x) {
+        uint32_t v;
+        asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p + i * 256));
+    }
+}
+
 __global__ void init_lru_kernel(uint16_t *lru, int64_t n, int B) {
     for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n;
          e += (int64_t)gridDim.x * blockDim.x)
@@ -142,6 +153,13 @@ cudaError_t launch_prefetch_copy(const DevPool &p, int layer, int n_req, int k, 
     if (x < 1) x = 1;
     prefetch_copy_kernel<<<dim3(x, n_req), kThreads, confined ? kConfinedSmem : 0, st>>>(
         p, layer, n_req, k, static_cast<const uint8_t *>(plan), plan_layer);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_touch(const void *p, size_t bytes, int sm_count, cudaStream_t st) {
+    if (bytes < 256) return cudaSuccess;
+    touch_kernel<<<(sm_count > 0 ? sm_count : 1) * 4, kThreads, 0, st>>>(
+        static_cast<const uint8_t *>(p), bytes);
     return cudaGetLastError();
 }
 

@@ -193,6 +193,29 @@ size_t thp_size() {
 
 int alloc_thp_registered(size_t bytes, int dev, HostBuffer *out);
 
+// Bytes of [p, p + n) that the kernel backs with transparent huge pages:
+// the AnonHugePages of the mappings overlapping it (/proc/self/smaps).
+size_t huge_backed_bytes(const void *p, size_t n) {
+    FILE *f = std::fopen("/proc/self/smaps", "r");
+    if (!f) return 0;
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p), hi = lo + n;
+    char line[512];
+    bool cur = false;
+    size_t kb = 0;
+    while (std::fgets(line, sizeof line, f)) {
+        unsigned long long a = 0, b = 0;
+        char c = 0;
+        if (std::sscanf(line, "%llx-%llx %c", &a, &b, &c) == 3) {  // a mapping's header line
+            cur = a < hi && b > lo;
+            continue;
+        }
+        unsigned long long v = 0;
+        if (cur && std::sscanf(line, "AnonHugePages: %llu kB", &v) == 1) kb += (size_t)v;
+    }
+    std::fclose(f);
+    return kb << 10;
+}
+
 }  // namespace
 
 int device_host_numa(int dev) {
@@ -249,6 +272,7 @@ int alloc_thp_registered(size_t bytes, int dev, HostBuffer *out) {
     out->bytes = bytes;
     out->mapped = size;
     out->granularity = hp;
+    out->huge_bytes = huge_backed_bytes(p, size);
     out->handle = reinterpret_cast<unsigned long long>(raw);
     out->kind = HS_HOST_ALLOC_THP_REGISTERED;
     out->numa = numa;

@@ -217,10 +217,11 @@ struct HostBuffer {
     const void *dev;
     size_t bytes;               // requested
     size_t mapped;              // allocated (rounded up to the granularity)
-    size_t granularity;         // VMM allocation granularity, 0 for cudaHostAlloc
-    unsigned long long handle;  // VMM allocation handle
-    int kind;                   // HS_HOST_ALLOC_PINNED or HS_HOST_ALLOC_VMM_NUMA
-    int numa;                   // node requested (VMM), -1 otherwise
+    size_t granularity;         // VMM granularity or huge-page size, 0 for cudaHostAlloc
+    size_t huge_bytes;          // bytes in transparent huge pages (huge-page kind)
+    unsigned long long handle;  // VMM allocation handle, or the huge-page mapping's start
+    int kind;                   // HS_HOST_ALLOC_*
+    int numa;                   // node requested, -1 otherwise
 };
 int host_alloc(size_t bytes, int kind, int dev, HostBuffer *out);
 int device_host_numa(int dev);
@@ -250,6 +251,7 @@ cudaError_t launch_prefetch_copy(const DevPool &p, int layer, int n_req, int k,
                                  const void *plan, int sm_count, cudaStream_t st,
                                  int plan_layer, bool confined);
 cudaError_t launch_init_lru(uint16_t *lru, int64_t pairs, int B, cudaStream_t st);
+cudaError_t launch_touch(const void *p, size_t bytes, int sm_count, cudaStream_t st);
 cudaError_t prepare_kernels(size_t max_smem);
 cudaError_t prepare_copy_kernel();
 cudaError_t launch_attention(const void *q, const void *cache, int64_t cache_rows,

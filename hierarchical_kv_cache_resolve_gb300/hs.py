@@ -125,6 +125,14 @@ def hs_device_host_numa(device: int) -> int:
     return int(_lib().hs_device_host_numa(device))
 
 
+def hs_touch_records(pool: int, req: int = -1, layer: int = -1, stream=None) -> None:
+    _check(_lib().hs_touch_records(pool, req, layer, _stream(stream)), "hs_touch_records")
+
+
+def hs_warm_pool(pool: int) -> None:
+    _check(_lib().hs_warm_pool(pool), "hs_warm_pool")
+
+
 def hs_pool_info(pool: int) -> dict:
     i = _native.PoolInfo()
     _check(_lib().hs_pool_info(pool, ctypes.byref(i)), "hs_pool_info")
@@ -273,6 +281,13 @@ class Pool:
 
     def info(self) -> dict:
         return hs_pool_info(self.handle)
+
+    def touch(self, req=-1, layer=-1, stream=None):
+        hs_touch_records(self.handle, req, layer, stream)
+
+    def warm(self):
+        """Touch every record, resolve synthetic steps, reset (before first use)."""
+        hs_warm_pool(self.handle)
 
     def close(self):
         if self.handle:

@@ -113,11 +113,14 @@ typedef struct {
 #define HS_OVERLAP_AUTO_MAX_HOST_BYTES (16ull << 30)
 
 /* ---- host pool memory (hs_pool_desc.host_alloc, hs_link_probe) --------- */
-/* The library's choice: HS_HOST_ALLOC_PINNED.  (Measured on GB300:
- * scattered 1152-byte GPU-thread reads of cudaHostAlloc memory run at the
- * full pinned-copy rate while the pool stays within the device's
- * translation reach, about 16 GiB; those of VMM host-NUMA memory at about
- * a fifth of it at any size.) */
+/* The library's choice: for pools of at most HS_OVERLAP_AUTO_MAX_HOST_BYTES
+ * of records, HS_HOST_ALLOC_PINNED; above, HS_HOST_ALLOC_THP_REGISTERED when
+ * the kernel backs at least 90 % of the pool with huge pages, else
+ * HS_HOST_ALLOC_PINNED.  (Measured on GB300: scattered 1152-byte GPU-thread
+ * reads of cudaHostAlloc memory run at the full pinned-copy rate while the
+ * pool stays within the device's translation reach, about 16 GiB, and
+ * collapse past it, where huge-page memory reads twice as fast; VMM
+ * host-NUMA memory reads at about a fifth of the rate at any size.) */
 #define HS_HOST_ALLOC_AUTO 0
 /* cudaHostAlloc(Mapped | Portable), made while the calling thread prefers
  * the host NUMA node closest to the device (set_mempolicy), so that the
@@ -132,10 +135,10 @@ typedef struct {
 /* Anonymous host memory in transparent huge pages (madvise on the mapping,
  * aligned to the huge-page size), first touched by threads preferring the
  * device's host NUMA node, then pinned and mapped for the device with
- * cudaHostRegister(Mapped | Portable).  Measured on GB300 with a 59 GB pool
- * in 512 MiB pages: scattered reads past the translation reach about twice
- * as fast as cudaHostAlloc memory once warm, but the first resolves over a
- * new pool run far slower (seconds), so it is not the default. */
+ * cudaHostRegister(Mapped | Portable).  Warm, it reads scattered records
+ * past the translation reach about twice as fast as cudaHostAlloc memory
+ * (measured on GB300); the first resolves over freshly written records are
+ * far slower (hs_touch_records, hs_warm_pool). */
 #define HS_HOST_ALLOC_THP_REGISTERED 3
 
 typedef struct {
@@ -203,10 +206,36 @@ typedef struct {
     uint64_t host_mapped_bytes;/* bytes allocated for them (granularity-rounded) */
     uint64_t host_granularity; /* VMM allocation granularity, 0 for cudaHostAlloc */
     uint64_t device_bytes;     /* bytes of device arrays the pool allocated */
+    uint64_t host_huge_bytes;  /* bytes of the host pool in transparent huge pages */
+    uint64_t warmup_us;        /* time the last hs_warm_pool took, µs (0: never called) */
 } hs_pool_info_t;
 
 /* Fills *out.  Errors: HS_ERR_INVALID_ARG (NULL pool or out). */
 int hs_pool_info(hs_pool *pool, hs_pool_info_t *out);
+
+/*
+ * Reads the host records of (req, layer) once from the device -- one
+ * 4-byte read per 256 bytes; req and/or layer -1 for all -- enqueued on
+ * `stream`.  Not part of the method: on GB300 the device's first read of
+ * host memory the CPU has written since is slow at 4 KiB granularity
+ * (measured on huge-page pools: the first resolve step over a freshly
+ * written 59 GB pool took 1.3 s, 30-100 ms after this call), so a caller
+ * that has just written records (prefill) can pay that here, off the
+ * latency-critical path.  Errors: HS_ERR_INVALID_ARG, HS_ERR_CUDA.
+ */
+int hs_touch_records(hs_pool *pool, int32_t req, int32_t layer, void *stream);
+
+/*
+ * Warms a pool after its records are written and before its first resolve:
+ * hs_touch_records of every record, then sixteen synthetic resolve steps
+ * through every (request, layer) pair (each step k new distinct positions
+ * per request, so that every selection misses), then the empty state of
+ * hs_create_pool again (hs_reset).  Synchronous; the time it took is
+ * hs_pool_info_t.warmup_us.  It discards the pool's slot state, so it must
+ * not be called once real resolves have run.  Errors: HS_ERR_INVALID_ARG,
+ * HS_ERR_NOMEM (its two small selection buffers), HS_ERR_CUDA.
+ */
+int hs_warm_pool(hs_pool *pool);
 
 /* Host NUMA node closest to CUDA device `device` (cudaDevAttrHostNumaId),
  * where a pool created on that device places its host records; -1 when

@@ -120,6 +120,8 @@ def test_calls_on_null_pool_are_rejected(lib):
     assert lib.hs_link_probe(8, 0, 1152, 0, None, None) == hs.HS_ERR_INVALID_ARG
     assert lib.hs_link_probe(1 << 20, 1, 1152, 7, None, None) == hs.HS_ERR_INVALID_ARG
     assert lib.hs_pool_info(None, None) == hs.HS_ERR_INVALID_ARG
+    assert lib.hs_touch_records(None, -1, -1, None) == hs.HS_ERR_INVALID_ARG
+    assert lib.hs_warm_pool(None) == hs.HS_ERR_INVALID_ARG
 
 
 def test_noalloc_refuses_misaligned_pointers_before_any_cuda_call(lib):

@@ -446,11 +446,25 @@ def test_pool_with_each_host_allocation(kind):
         info = pool.info()
         assert info["host_alloc"] == kind
         assert info["launch_overlap"] == hs.HS_OVERLAP_ON   # a small pool overlaps by default
+        assert info["warmup_us"] == 0
         assert info["host_bytes"] == w.host_bytes and info["host_mapped_bytes"] >= w.host_bytes
         if kind == hs.HS_HOST_ALLOC_VMM_NUMA and info["device_numa"] >= 0 \
                 and info["host_numa_first"] >= 0:
             assert info["host_numa_first"] == info["device_numa"]
         fill_selected(pool, w, sel)
+        # touch some records, then warm the whole pool: the warm-up resolves
+        # synthetic steps and leaves the pool as created
+        pool.touch(1, 0)
+        pool.touch(-1, 1)
+        pool.touch(2, -1)
+        pool.warm()
+        assert pool.info()["warmup_us"] > 0
+        st = pool.stats()
+        assert st["resolves"] == 0 and st["misses"] == 0 and st["status"] == 0
+        for l in range(w.n_layers):
+            v = pool.views(l)
+            assert (v["slot_pos"] == -1).all() and (v["page_table"] == -1).all()
+            assert (v["resolves"] == 0).all()
         out = torch.empty((w.n_requests, w.k), dtype=torch.int32, device="cuda")
         for t in range(w.steps):
             for l in range(w.n_layers):

@@ -231,8 +231,15 @@ def test_tight_prefetch_full_as_the_benchmark_runs_it():
     orc = OracleRun(w)
     ex = ThreadPoolExecutor(16)
     with hs.Pool.for_workload(w) as pool:
-        assert pool.info()["launch_overlap"] == hs.HS_OVERLAP_OFF
+        info = pool.info()
+        assert info["launch_overlap"] == hs.HS_OVERLAP_OFF
+        # past the translation reach the pool takes huge pages when the kernel
+        # backs nearly all of it with them; the bench warms it once written
+        assert info["host_alloc"] in (hs.HS_HOST_ALLOC_THP_REGISTERED, hs.HS_HOST_ALLOC_PINNED)
+        if info["host_alloc"] == hs.HS_HOST_ALLOC_THP_REGISTERED:
+            assert info["host_huge_bytes"] >= info["host_mapped_bytes"] // 10 * 9
         fill_selected(pool, w, sel)
+        pool.warm()
         dsel = device_trace(sel)
         out = torch.empty((T, NL, R, k), dtype=torch.int32, device="cuda")
         flush = torch.empty(64 << 20, dtype=torch.int32, device="cuda")

@@ -40,6 +40,7 @@ void free_device(hs_pool *p) {
     cudaFree(p->dp.busy);
     cudaFree(p->dp.counters);
     cudaFree(p->dp.status);
+    cudaFree(p->dp.sink);
     hs::host_free(&p->host);
 }
 
@@ -248,7 +249,7 @@ int hs_create_pool(const hs_pool_desc *desc, hs_pool **out) {
         !cuda_ok(cudaMalloc(&p->dp.tcount, pairs * 4)) ||
         !cuda_ok(cudaMalloc(&p->dp.busy, pairs * 4)) ||
         !cuda_ok(cudaMalloc(&p->dp.counters, (size_t)d.n_layers * hs::CTR_COUNT * 8)) ||
-        !cuda_ok(cudaMalloc(&p->dp.status, 4))) {
+        !cuda_ok(cudaMalloc(&p->dp.status, 4)) || !cuda_ok(cudaMalloc(&p->dp.sink, 4))) {
         cudaGetLastError();
         rc = HS_ERR_NOMEM;
         goto fail;
@@ -300,13 +301,15 @@ int hs_touch_records(hs_pool *pool, int32_t req, int32_t layer, void *stream) {
     // contiguous; one (request, layer) region otherwise
     cudaError_t e = cudaSuccess;
     if (req < 0 && layer < 0) {
-        e = hs::launch_touch(base, pool->host_bytes, pool->sm_count, st);
+        e = hs::launch_touch(base, pool->host_bytes, pool->dp.sink, pool->sm_count, st);
     } else if (layer < 0) {
-        e = hs::launch_touch(base + (size_t)req * NL * per, (size_t)NL * per, pool->sm_count, st);
+        e = hs::launch_touch(base + (size_t)req * NL * per, (size_t)NL * per, pool->dp.sink,
+                             pool->sm_count, st);
     } else {
         for (int r = (req < 0 ? 0 : req); r < (req < 0 ? pool->desc.n_requests : req + 1) &&
                                            e == cudaSuccess; ++r)
-            e = hs::launch_touch(base + ((size_t)r * NL + layer) * per, per, pool->sm_count, st);
+            e = hs::launch_touch(base + ((size_t)r * NL + layer) * per, per, pool->dp.sink,
+                                 pool->sm_count, st);
     }
     return cuda_ok(e) ? HS_OK : HS_ERR_CUDA;
 }

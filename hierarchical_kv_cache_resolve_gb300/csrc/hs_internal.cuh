@@ -50,6 +50,7 @@ struct DevPool {
     uint32_t *busy;
     unsigned long long *counters;
     unsigned int *status;
+    uint32_t *sink;  // a word only the touch kernel may write (never read)
     int32_t R, NL, B, W;
     int64_t L;
 };
@@ -251,7 +252,8 @@ cudaError_t launch_prefetch_copy(const DevPool &p, int layer, int n_req, int k,
                                  const void *plan, int sm_count, cudaStream_t st,
                                  int plan_layer, bool confined);
 cudaError_t launch_init_lru(uint16_t *lru, int64_t pairs, int B, cudaStream_t st);
-cudaError_t launch_touch(const void *p, size_t bytes, int sm_count, cudaStream_t st);
+cudaError_t launch_touch(const void *p, size_t bytes, uint32_t *sink, int sm_count,
+                         cudaStream_t st);
 cudaError_t prepare_kernels(size_t max_smem);
 cudaError_t prepare_copy_kernel();
 cudaError_t launch_attention(const void *q, const void *cache, int64_t cache_rows,

@@ -236,8 +236,7 @@ namespace {
 int alloc_thp_registered(size_t bytes, int dev, HostBuffer *out) {
     const size_t hp = thp_size();
     const size_t size = (bytes + hp - 1) / hp * hp;
-    void *raw = mmap(nullptr, size + hp, PROT_READ | PROT_WRITE,
-                     MAP_PRIVATE | MAP_ANONYMOUS | MAP_NORESERVE, -1, 0);
+    void *raw = mmap(nullptr, size + hp, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
     if (raw == MAP_FAILED) return HS_ERR_NOMEM;
     uint8_t *p = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(raw) + hp - 1) / hp * hp);
@@ -249,12 +248,18 @@ int alloc_thp_registered(size_t bytes, int dev, HostBuffer *out) {
     if (nt < 1) nt = 1;
     if (nt > 64) nt = 64;
     if ((size_t)nt > pages) nt = (unsigned)pages;
+    auto touch_share = [=](unsigned t) {
+        PreferNode prefer(numa);
+        for (size_t i = t; i < pages; i += nt) std::memset(p + i * hp, 0, hp);
+    };
     std::vector<std::thread> th;
-    for (unsigned t = 0; t < nt; ++t)
-        th.emplace_back([=] {
-            PreferNode prefer(numa);
-            for (size_t i = t; i < pages; i += nt) std::memset(p + i * hp, 0, hp);
-        });
+    unsigned started = 0;
+    try {
+        for (; started < nt; ++started) th.emplace_back(touch_share, started);
+    } catch (...) {
+        // no more threads: this one touches the shares left
+    }
+    for (unsigned t = started; t < nt; ++t) touch_share(t);
     for (auto &x : th) x.join();
     if (cudaHostRegister(p, size, cudaHostRegisterMapped | cudaHostRegisterPortable) != cudaSuccess) {
         cudaGetLastError();

@@ -417,10 +417,6 @@ def run_gpu(args, w, rank, world, dist_on, lite=False):
             records.fill(pool.host_records(r, l).ctypes.data, w, r, l)
     pool_info["create_and_fill_s"] = time.perf_counter() - t_fill
     h2d_gbs, gather_gbs = hs.hs_link_probe(1 << 30, 10, W, kind)
-    # the records are written: read them once from the device and resolve
-    # synthetic steps, then reset (hs_warm_pool; outside every timed region)
-    pool.warm()
-    pool_info["warmup_us"] = pool.info()["warmup_us"]
     base_addr = pool.host_records(0, 0).ctypes.data
     pool_info["pages"] = host_pages(base_addr, w.host_bytes)
     pool_info["host_address"] = hex(base_addr)
@@ -452,6 +448,11 @@ def run_gpu(args, w, rank, world, dist_on, lite=False):
             for l in range(NL):
                 hs.hs_resolve(pool.handle, l, R, None, dsel[t, l], k, out[l], None, cap)
         graphs.append(g)
+    # the records are written and the graphs captured: read the records once
+    # from the device and resolve synthetic steps, then reset (hs_warm_pool;
+    # outside every timed region, right before the steps)
+    pool.warm()
+    pool_info["warmup_us"] = pool.info()["warmup_us"]
     # step 0 from an empty cache (every selection misses), timed on its own;
     # it is the first of the warm-up steps
     flush(0)

@@ -317,9 +317,7 @@ int hs_touch_records(hs_pool *pool, int32_t req, int32_t layer, void *stream) {
 int hs_warm_pool(hs_pool *pool) {
     if (!pool) return HS_ERR_INVALID_ARG;
     const auto t0 = std::chrono::steady_clock::now();
-    int rc = hs_touch_records(pool, -1, -1, nullptr);
-    if (rc == HS_OK && !cuda_ok(cudaDeviceSynchronize())) rc = HS_ERR_CUDA;
-    if (rc == HS_OK) rc = warm_pool(pool);
+    const int rc = warm_pool(pool);
     if (rc == HS_OK)
         pool->warmup_us =
             std::chrono::duration<double, std::micro>(std::chrono::steady_clock::now() - t0).count();

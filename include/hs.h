@@ -227,13 +227,15 @@ int hs_touch_records(hs_pool *pool, int32_t req, int32_t layer, void *stream);
 
 /*
  * Warms a pool after its records are written and before its first resolve:
- * hs_touch_records of every record, then sixteen synthetic resolve steps
- * through every (request, layer) pair (each step k new distinct positions
- * per request, so that every selection misses), then the empty state of
- * hs_create_pool again (hs_reset).  Synchronous; the time it took is
- * hs_pool_info_t.warmup_us.  It discards the pool's slot state, so it must
- * not be called once real resolves have run.  Errors: HS_ERR_INVALID_ARG,
- * HS_ERR_NOMEM (its two small selection buffers), HS_ERR_CUDA.
+ * sixteen synthetic resolve steps through every (request, layer) pair (each
+ * step k new distinct positions per request, so that every selection misses
+ * and every slot is written), then the empty state of hs_create_pool again
+ * (hs_reset).  Not part of the method: on GB300 the first resolve step over
+ * a freshly written 59 GB huge-page pool took 1.3-3.1 s, after this call
+ * 7-43 ms.  Synchronous; the time it took is hs_pool_info_t.warmup_us.  It
+ * discards the pool's slot state, so it must not be called once real
+ * resolves have run.  Errors: HS_ERR_INVALID_ARG, HS_ERR_NOMEM (its two
+ * small selection buffers), HS_ERR_CUDA.
  */
 int hs_warm_pool(hs_pool *pool);
 

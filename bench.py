@@ -1457,6 +1457,18 @@ def bind_to_device_numa(device: int):
         return node, None
 
 
+def host_memory_available():
+    """MemAvailable of /proc/meminfo in bytes (None if unknown)."""
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except (OSError, ValueError, IndexError):
+        pass
+    return None
+
+
 def parse_cpulist(text: str) -> set:
     """'0-3,8,10-11' -> {0, 1, 2, 3, 8, 10, 11}"""
     cpus = set()
@@ -1570,6 +1582,11 @@ def main(argv=None):
     dist_on = world > 1
     if not torch.cuda.is_available():
         raise SystemExit("bench.py: no CUDA device (the resolve path has no CPU fallback)")
+    need = max([base.host_bytes] + [shaped(n).host_bytes for n in also]) * world
+    avail = host_memory_available()
+    if avail is not None and need > avail:
+        raise SystemExit(f"bench.py: {world} rank(s) need {need / 1e9:.1f} GB of pinned host "
+                         f"memory for their pools, {avail / 1e9:.1f} GB is available")
     torch.cuda.set_device(local)
     numa, numa_cpus = bind_to_device_numa(local)
     if dist_on:

@@ -67,10 +67,10 @@ int reset_state(hs_pool *p) {
 int pick_cluster(const hs_pool *p, int n_req);
 int lead_share(const hs_pool *p, int k, int cluster);
 
-// Synthetic resolves over every (request, layer) pair, then the empty
-// state again (hs_warm_pool): kWarmSteps steps, each a new set of k
-// distinct positions per request, so that every selection misses and every
-// slot is written.
+// Every byte of the host records read once from the device, synthetic
+// resolves over every (request, layer) pair, then the empty state again
+// (hs_warm_pool): kWarmSteps steps, each a new set of k distinct positions
+// per request, so that every selection misses and every slot is written.
 constexpr int kWarmSteps = 16;
 int warm_pool(hs_pool *p) {
     const int R = p->desc.n_requests, NL = p->desc.n_layers;
@@ -83,6 +83,9 @@ int warm_pool(hs_pool *p) {
     if (!cuda_ok(cudaMalloc(&dsel, sel.size() * 4)) || !cuda_ok(cudaMalloc(&dout, sel.size() * 4))) {
         rc = HS_ERR_NOMEM;
     } else {
+        // every byte of the records read once, then the synthetic steps
+        if (!cuda_ok(hs::launch_touch(p->host.dev, p->host_bytes, p->dp.sink, p->sm_count, 0)))
+            rc = HS_ERR_CUDA;
         const int cluster = pick_cluster(p, R);
         for (int step = 0; step < kWarmSteps && rc == HS_OK; ++step) {
             // positions (base_r + step * D + i * G) mod L: distinct, since k * G <= L

@@ -89,18 +89,18 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
-// One 4-byte device read of every 256 bytes of [p, p + bytes).  The words
-// are folded into a value that is stored to `sink` only if it equals a
-// constant, so that no compiler stage may drop the reads as dead; `sink`
-// is a word no one else reads.
+// Reads every byte of [p, p + bytes) once from the device (16-byte loads;
+// `bytes` a multiple of 16, p 16-byte aligned).  The words are folded into
+// a value that is stored to `sink` only if it equals a constant, so that no
+// compiler stage may drop the reads as dead; `sink` is a word no one else
+// reads.
 __global__ void touch_kernel(const uint8_t *__restrict__ p, size_t bytes, uint32_t *sink) {
-    const size_t n = bytes / 256;
+    const size_t n = bytes / 16;
     uint32_t acc = 0;
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
          i += (size_t)gridDim.x * blockDim.x) {
-        uint32_t v;
-        asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p + i * 256));
-        acc = acc * 31u + v;
+        const uint4 v = ld_nc_v4(p + i * 16);
+        acc = acc * 31u + (v.x ^ v.y ^ v.z ^ v.w);
     }
     if (acc == 0x9E3779B9u) *sink = acc;
 }
@@ -163,7 +163,7 @@ cudaError_t launch_prefetch_copy(const DevPool &p, int layer, int n_req, int k, 
 
 cudaError_t launch_touch(const void *p, size_t bytes, uint32_t *sink, int sm_count,
                          cudaStream_t st) {
-    if (bytes < 256) return cudaSuccess;
+    if (bytes < 16) return cudaSuccess;
     touch_kernel<<<(sm_count > 0 ? sm_count : 1) * 4, kThreads, 0, st>>>(
         static_cast<const uint8_t *>(p), bytes, sink);
     return cudaGetLastError();

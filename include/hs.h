@@ -214,25 +214,26 @@ typedef struct {
 int hs_pool_info(hs_pool *pool, hs_pool_info_t *out);
 
 /*
- * Reads the host records of (req, layer) once from the device -- one
- * 4-byte read per 256 bytes; req and/or layer -1 for all -- enqueued on
- * `stream`.  Not part of the method: on GB300 the device's first read of
- * host memory the CPU has written since is slow at 4 KiB granularity
- * (measured on huge-page pools: the first resolve step over a freshly
- * written 59 GB pool took 1.3 s, 30-100 ms after this call), so a caller
- * that has just written records (prefill) can pay that here, off the
- * latency-critical path.  Errors: HS_ERR_INVALID_ARG, HS_ERR_CUDA.
+ * Reads every byte of the host records of (req, layer) once from the device
+ * (16-byte loads; req and/or layer -1 for all), enqueued on `stream`.  Not
+ * part of the method: on GB300 the device's first reads of host records the
+ * CPU has just written are slow, so a caller that has just written records
+ * (prefill) can pay that here, off the latency-critical path (measured:
+ * 59 GB of a freshly written huge-page pool in 1.5-1.8 s).
+ * Errors: HS_ERR_INVALID_ARG, HS_ERR_CUDA.
  */
 int hs_touch_records(hs_pool *pool, int32_t req, int32_t layer, void *stream);
 
 /*
  * Warms a pool after its records are written and before its first resolve:
- * sixteen synthetic resolve steps through every (request, layer) pair (each
- * step k new distinct positions per request, so that every selection misses
- * and every slot is written), then the empty state of hs_create_pool again
+ * every byte of the host records read once (hs_touch_records), sixteen
+ * synthetic resolve steps through every (request, layer) pair (each step k
+ * new distinct positions per request, so that every selection misses and
+ * every slot is written), then the empty state of hs_create_pool again
  * (hs_reset).  Not part of the method: on GB300 the first resolve step over
- * a freshly written 59 GB huge-page pool took 1.3-3.1 s, after this call
- * 7-43 ms.  Synchronous; the time it took is hs_pool_info_t.warmup_us.  It
+ * a freshly written 59 GB huge-page pool took 1.3-3.1 s cold, 54-61 ms
+ * after the synthetic steps alone and 7-50 ms after this call (2.0-2.1 s in
+ * all).  Synchronous; the time it took is hs_pool_info_t.warmup_us.  It
  * discards the pool's slot state, so it must not be called once real
  * resolves have run.  Errors: HS_ERR_INVALID_ARG, HS_ERR_NOMEM (its two
  * small selection buffers), HS_ERR_CUDA.

@@ -1081,7 +1081,7 @@ cudaError_t launch_variant(const DevPool &p, int layer, int n_req, const int32_t
     cfg.gridDim = dim3((unsigned)(n_req * cluster), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     // A plain launch takes all the shared memory a CTA may have: the CTA is
-    // alone on its SM anyway (512 threads x 72 registers), and the followers
+    // alone on its SM anyway (512 threads x 96 registers), and the followers
     // stage more records before the leader decides.
     uint32_t smem = resolve_smem_bytes(p.B, k, plan != nullptr, p.L);
     if (!plan) {

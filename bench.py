@@ -537,6 +537,7 @@ def run_gpu(args, w, rank, world, dist_on, lite=False):
                          "avg_launch_us": avg_launch_s * 1e6},
             "repeats": [len(g) * R * NL / (sum(g) / 1e3)
                         for g in np.array_split(np.array(step_ms), 3) if len(g)],
+            "step_ms": step_time_summary(step_ms, R * NL),
             "cold_step_ms": cold_ms, "host_pool": pool_info,
             "l2": "flushed before every timed step"}
 
@@ -746,6 +747,7 @@ def run_gpu(args, w, rank, world, dist_on, lite=False):
             "resolves_per_s": [len(g) * R * NL / (sum(g) / 1e3)
                                for g in np.array_split(np.array(step_ms), 3) if len(g)],
         },
+        "step_ms": step_time_summary(step_ms, R * NL),
         "cold_step": {
             "what": "step 0 from an empty cache (every selection misses), one graph replay, "
                     "L2 flushed; not in `value`",
@@ -760,6 +762,21 @@ def run_gpu(args, w, rank, world, dist_on, lite=False):
         "graph_wall_s": wall_graph,
     }
     return res
+
+
+def step_time_summary(step_ms, resolves_per_step):
+    """Distribution of the timed steps' device times (rank 0), beside the
+    mean that `value` is: the median step is the steady rate, the upper
+    ones show steps slowed by the host (stalls after a pool is created or
+    the GPU has idled).  Not a replacement for `value`."""
+    a = np.sort(np.asarray(step_ms, dtype=np.float64))
+    if a.size == 0:
+        return None
+    med = float(np.median(a))
+    return {"what": "device time of each timed step (rank 0), ms; `value` is the mean rate",
+            "min": float(a[0]), "median": med, "p90": float(np.percentile(a, 90)),
+            "max": float(a[-1]),
+            "resolves_per_s_at_median": resolves_per_step / (med / 1e3) if med > 0 else None}
 
 
 def _timed_graph_steps(graphs, flush, main):

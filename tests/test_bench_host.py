@@ -139,3 +139,11 @@ def test_bind_without_device_reports_no_node():
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert bench.bind_to_device_numa(0) == (None, None)
+
+
+def test_step_time_summary():
+    st = bench.step_time_summary([1.0, 0.99, 1.5, 0.98, 2.0], 512)
+    assert st["min"] == 0.98 and st["median"] == 1.0 and st["max"] == 2.0
+    assert abs(st["resolves_per_s_at_median"] - 512 / 1e-3) < 1e-6
+    assert st["min"] <= st["p90"] <= st["max"]
+    assert bench.step_time_summary([], 512) is None

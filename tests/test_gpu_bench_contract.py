@@ -51,3 +51,8 @@ def test_default_bench_line():
     assert d["no_fetch"]["status"] == 0 and d["stages"]["status"] == 0
     assert d["no_fetch"]["roofline_hbm_metadata"]["bound"] == "hbm"
     assert "dsa_mla" in d["other_workloads"]
+    # the step-time distribution beside the mean step that `value` is
+    st = d["step_ms"]
+    assert st["min"] <= st["median"] <= st["p90"] <= st["max"]
+    assert st["min"] * (1 - 1e-9) <= d["ms_per_step"] <= st["max"] * (1 + 1e-9)
+    assert st["resolves_per_s_at_median"] > 0

@@ -32,9 +32,8 @@
 // the value columns, in a fixed order.
 //
 // The work is bound by the gathered bytes (about 30 flops per byte at 16
-// heads), so the kernel is built around keeping the gather busy: a split
-// count chosen so that the grid covers the GPU once, one CTA per SM when
-// that allows as many splits as two per SM would, two otherwise.
+// heads), so the kernel is built around keeping the gather busy: two CTAs
+// per SM, and a split count chosen so that the grid covers the GPU once.
 #include <algorithm>
 #include <cstdint>
 #include <mutex>
@@ -520,31 +519,21 @@ __global__ void __launch_bounds__(kAttnThreads, 2)
     cluster.sync();  // no CTA leaves while another still reads its shared memory
 }
 
-// Dynamic shared memory a launch asks for when its grid fits one CTA per
-// SM: more than half of an SM's, so that no two CTAs share one (the kernel
-// uses kAttnSmem of it).  Without it the 16-CTA clusters of a small batch
-// were placed two CTAs to an SM while other SMs stayed idle.
-constexpr uint32_t kAttnSmemAlone = 120 * 1024;
-static_assert(kAttnSmemAlone >= kAttnSmem, "the alone request covers the kernel's layout");
-
 struct DeviceInfo {
     int dev = -1, sms = 0;
-    int active[5] = {0, 0, 0, 0, 0};   // co-resident clusters of 1, 2, 4, 8, 16 CTAs
-    int active1[5] = {0, 0, 0, 0, 0};  // the same with one CTA per SM (kAttnSmemAlone)
+    int active[5] = {0, 0, 0, 0, 0};  // co-resident clusters of 1, 2, 4, 8, 16 CTAs
 };
 
 // Splits per (request, head group) -- the cluster size: a power of two, no
 // more than ceil(k / 64), and the largest whose clusters for all the units
 // are co-resident (one wave), never more CTAs than two per SM.
-int nsplit_for(int n_req, int k, int heads, const DeviceInfo &di, bool alone) {
+int nsplit_for(int n_req, int k, int heads, const DeviceInfo &di) {
     const int64_t units = (int64_t)n_req * (heads / kGroup);
     const int max_split = (k + kMinSplitKeys - 1) / kMinSplitKeys;
-    const int64_t per_sm = alone ? 1 : 2;
-    const int *active = alone ? di.active1 : di.active;
     int n = 1;
     for (int e = 1; e < 5; ++e) {
         const int c = 1 << e;
-        if (c > max_split || units * c > per_sm * di.sms || units > active[e]) break;
+        if (c > max_split || units * c > 2 * (int64_t)di.sms || units > di.active[e]) break;
         n = c;
     }
     return n;
@@ -566,33 +555,31 @@ cudaError_t device_info(DeviceInfo *out) {
         e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kAttnSmemAlone);
+                                 (int)kAttnSmem);
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
         if (e != cudaSuccess) return e;
         const bool big = cudaFuncSetAttribute(
                              attn_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
                          cudaSuccess;
-        for (int alone = 0; alone < 2; ++alone)
-            for (int e = 0; e < 5; ++e) {
-                const int c = 1 << e;
-                if (c > 8 && !big) break;
-                cudaLaunchConfig_t cfg = {};
-                cfg.gridDim = dim3(c, 1, 1);
-                cfg.blockDim = dim3(kAttnThreads);
-                cfg.dynamicSmemBytes = alone ? kAttnSmemAlone : kAttnSmem;
-                cudaLaunchAttribute attr[1];
-                attr[0].id = cudaLaunchAttributeClusterDimension;
-                attr[0].val.clusterDim.x = c;
-                attr[0].val.clusterDim.y = 1;
-                attr[0].val.clusterDim.z = 1;
-                cfg.attrs = attr;
-                cfg.numAttrs = 1;
-                int clusters = 0;
-                if (cudaOccupancyMaxActiveClusters(&clusters, attn_kernel, &cfg) != cudaSuccess)
-                    break;
-                (alone ? d.active1 : d.active)[e] = clusters;
-            }
+        for (int e = 0; e < 5; ++e) {
+            const int c = 1 << e;
+            if (c > 8 && !big) break;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(c, 1, 1);
+            cfg.blockDim = dim3(kAttnThreads);
+            cfg.dynamicSmemBytes = kAttnSmem;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = c;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int clusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&clusters, attn_kernel, &cfg) != cudaSuccess) break;
+            d.active[e] = clusters;
+        }
         (void)cudaGetLastError();  // a refused query above leaves no sticky error
         cached = d;
     }
@@ -608,17 +595,13 @@ cudaError_t launch_attention(const void *q, const void *cache, int64_t cache_row
     DeviceInfo di;
     cudaError_t e = device_info(&di);
     if (e != cudaSuccess) return e;
-    // one CTA per SM when that gives as many splits as two per SM would
-    const int n_alone = nsplit_for(n_req, k, heads, di, true);
-    const int n_pair = nsplit_for(n_req, k, heads, di, false);
-    const bool alone = n_alone >= n_pair;
-    const int nsplit = alone ? n_alone : n_pair;
+    const int nsplit = nsplit_for(n_req, k, heads, di);
     const int stages = (k + kStageKeys - 1) / kStageKeys;
     const int split_keys = ((stages + nsplit - 1) / nsplit) * kStageKeys;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(nsplit, n_req, heads / kGroup);
     cfg.blockDim = dim3(kAttnThreads);
-    cfg.dynamicSmemBytes = alone ? kAttnSmemAlone : kAttnSmem;
+    cfg.dynamicSmemBytes = kAttnSmem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;

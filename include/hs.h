@@ -232,8 +232,8 @@ int hs_touch_records(hs_pool *pool, int32_t req, int32_t layer, void *stream);
  * every slot is written), then the empty state of hs_create_pool again
  * (hs_reset).  Not part of the method: on GB300 the first resolve step over
  * a freshly written 59 GB huge-page pool took 1.3-3.1 s cold, 54-61 ms
- * after the synthetic steps alone and 7-50 ms after this call (2.0-2.1 s in
- * all).  Synchronous; the time it took is hs_pool_info_t.warmup_us.  It
+ * after the synthetic steps alone and 7-98 ms after this call, depending on
+ * the pool instance (2.0-2.9 s in all).  Synchronous; the time it took is hs_pool_info_t.warmup_us.  It
  * discards the pool's slot state, so it must not be called once real
  * resolves have run.  Errors: HS_ERR_INVALID_ARG, HS_ERR_NOMEM (its two
  * small selection buffers), HS_ERR_CUDA.

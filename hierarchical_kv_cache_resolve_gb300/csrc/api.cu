@@ -287,8 +287,9 @@ int hs_host_records(hs_pool *pool, int32_t req, int32_t layer, void **host_ptr) 
     if (!pool || !host_ptr || req < 0 || req >= pool->desc.n_requests || layer < 0 ||
         layer >= pool->desc.n_layers)
         return HS_ERR_INVALID_ARG;
-    const size_t per = (size_t)pool->desc.n_positions * pool->desc.record_bytes;
-    *host_ptr = static_cast<uint8_t *>(pool->host.host) + ((size_t)req * pool->desc.n_layers + layer) * per;
+    *host_ptr = static_cast<uint8_t *>(pool->host.host) +
+                hs::host_region(req, layer, pool->desc.n_requests, pool->desc.n_positions,
+                                pool->desc.record_bytes);
     return HS_OK;
 }
 
@@ -297,22 +298,23 @@ int hs_touch_records(hs_pool *pool, int32_t req, int32_t layer, void *stream) {
         layer >= pool->desc.n_layers)
         return HS_ERR_INVALID_ARG;
     const size_t per = (size_t)pool->desc.n_positions * pool->desc.record_bytes;
-    const int NL = pool->desc.n_layers;
+    const int R = pool->desc.n_requests, NL = pool->desc.n_layers;
     const uint8_t *base = static_cast<const uint8_t *>(pool->host.dev);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // host[r][l][L][W]: all of a request's layers, or all requests, are
+    auto region = [&](int r, int l) {
+        return base + hs::host_region(r, l, R, pool->desc.n_positions, pool->desc.record_bytes);
+    };
+    // host[l][r][L][W]: all of a layer's requests, or all layers, are
     // contiguous; one (request, layer) region otherwise
     cudaError_t e = cudaSuccess;
     if (req < 0 && layer < 0) {
         e = hs::launch_touch(base, pool->host_bytes, pool->dp.sink, pool->sm_count, st);
-    } else if (layer < 0) {
-        e = hs::launch_touch(base + (size_t)req * NL * per, (size_t)NL * per, pool->dp.sink,
-                             pool->sm_count, st);
+    } else if (req < 0) {
+        e = hs::launch_touch(region(0, layer), (size_t)R * per, pool->dp.sink, pool->sm_count, st);
     } else {
-        for (int r = (req < 0 ? 0 : req); r < (req < 0 ? pool->desc.n_requests : req + 1) &&
-                                           e == cudaSuccess; ++r)
-            e = hs::launch_touch(base + ((size_t)r * NL + layer) * per, per, pool->dp.sink,
-                                 pool->sm_count, st);
+        for (int l = (layer < 0 ? 0 : layer); l < (layer < 0 ? NL : layer + 1) && e == cudaSuccess;
+             ++l)
+            e = hs::launch_touch(region(req, l), per, pool->dp.sink, pool->sm_count, st);
     }
     return cuda_ok(e) ? HS_OK : HS_ERR_CUDA;
 }

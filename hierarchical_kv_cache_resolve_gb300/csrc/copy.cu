@@ -42,7 +42,7 @@ __global__ void __launch_bounds__(kThreads)
     const int32_t *ppos = eh + 4;
     const int32_t *pslot = ppos + k;
     const int W = p.W, B = p.B, CW = W >> 4;
-    const uint8_t *host_pair = p.host + ((int64_t)r * p.NL + layer) * p.L * W;
+    const uint8_t *host_pair = p.host + host_region(r, layer, p.R, p.L, W);
     uint8_t *cache_pair = p.cache + ((int64_t)layer * p.R + r) * B * (int64_t)W;
 
     if (blockIdx.x == 0) {

@@ -13,7 +13,7 @@
 //   busy     [N_l][R]        u32    1 while a resolve owns the pair
 //   counters [N_l][8]        u64    see CTR_*
 //   status   [1]             u32    HS_STATUS_* bits
-// Host pool (pinned, device-mapped): host[R][N_l][L][W].
+// Host pool (pinned, device-mapped): host[N_l][R][L][W] (host_region).
 #pragma once
 
 #include <cstddef>
@@ -54,6 +54,12 @@ struct DevPool {
     int32_t R, NL, B, W;
     int64_t L;
 };
+
+// Host records of (request r, layer l): the pool is layer-major,
+// [N_l][R][L][W], so that one layer's launch reads one contiguous range.
+__host__ __device__ inline int64_t host_region(int r, int l, int R, int64_t L, int W) {
+    return ((int64_t)l * R + r) * L * W;
+}
 
 // Plan buffer: a 16-byte header {magic, n_req, k, layer}, then per request
 // i an entry of 16 + 8k bytes: {m, req, 0, 0}, pos[k], slot[k].

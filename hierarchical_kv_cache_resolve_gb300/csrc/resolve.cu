@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int r = req_ids ? req_ids[ireq] : ireq;
     bool r_ok = r >= 0 && r < p.R;
     int64_t pair = (int64_t)layer * p.R + (r_ok ? r : 0);
-    const uint8_t *host_pair = p.host + ((int64_t)(r_ok ? r : 0) * p.NL + layer) * p.L * W;
+    const uint8_t *host_pair = p.host + host_region(r_ok ? r : 0, layer, p.R, p.L, W);
     uint8_t *cache_pair = p.cache + pair * B * (int64_t)W;
 
     if (crank == 0) {
@@ -658,7 +658,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             r = r_now;
             r_ok = r >= 0 && r < p.R;
             pair = (int64_t)layer * p.R + (r_ok ? r : 0);
-            host_pair = p.host + ((int64_t)(r_ok ? r : 0) * p.NL + layer) * p.L * W;
+            host_pair = p.host + host_region(r_ok ? r : 0, layer, p.R, p.L, W);
             cache_pair = p.cache + pair * B * (int64_t)W;
         }  // attempts
         const uint32_t abort_bits = hdr[H_ABORT];
@@ -771,7 +771,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             r = r_now;
             r_ok = r >= 0 && r < p.R;
             pair = (int64_t)layer * p.R + (r_ok ? r : 0);
-            host_pair = p.host + ((int64_t)(r_ok ? r : 0) * p.NL + layer) * p.L * W;
+            host_pair = p.host + host_region(r_ok ? r : 0, layer, p.R, p.L, W);
             cache_pair = p.cache + pair * B * (int64_t)W;
             __syncthreads();  // every warp is done staging
             if (tid == 0) hdr[H_NSTG] = 0u;

@@ -168,7 +168,8 @@ typedef struct {
 
 /*
  * Creates a pool: allocates the pinned, device-mapped host pool
- * (R * N_l * L_ctx * W bytes, host[r][l][pos][W], left uninitialised) and
+ * (R * N_l * L_ctx * W bytes, layer-major host[l][r][pos][W] -- one layer's
+ * records one contiguous range -- left uninitialised) and
  * the device arrays: cache (N_l * R * B * W bytes), page tables
  * (N_l * R * L_ctx * 4 bytes), slot maps, stamps, LRU orders, counters.
  * All slots start empty, every page-table entry host-only, every stamp 0.
@@ -387,12 +388,12 @@ int hs_prefetch_plan(hs_pool *pool, int32_t anchor_layer, int32_t target_layer,
                      int32_t k, void *d_plan, void *stream);
 
 /*
- * Exact layer-wise prefetch, copy half: a copy-only kernel that writes
- * host[r][target_layer][pos] into slot `slot` of request r for every pair of
- * d_plan (n_req, k as given to hs_prefetch_plan or hs_resolve_anchor; a
- * plan of target_layer or of its anchor layer).  Meant for a side stream
- * so that the transfer overlaps other work (notes, section 4).  It touches
- * no metadata: the consuming hs_resolve commits it.
+ * Exact layer-wise prefetch, copy half: a copy-only kernel that writes the
+ * host record (r, target_layer, pos) into slot `slot` of request r for
+ * every pair of d_plan (n_req, k as given to hs_prefetch_plan or
+ * hs_resolve_anchor; a plan of target_layer or of its anchor layer).
+ * Meant for a side stream so that the transfer overlaps other work (notes,
+ * section 4).  It touches no metadata: the consuming hs_resolve commits it.
  */
 int hs_prefetch_copy(hs_pool *pool, int32_t target_layer, int32_t n_req, int32_t k,
                      const void *d_plan, void *stream);

@@ -481,10 +481,13 @@ def test_host_records_layout():
     w = _small()
     with hs.Pool.for_workload(w) as pool:
         a = pool.host_records(1, 1)
-        b = pool.host_records(2, 0)
         assert a.shape == (w.n_positions, w.record_bytes)
-        gap = b.ctypes.data - a.ctypes.data
-        assert gap == w.n_positions * w.record_bytes   # host[r][l][pos][W]
+        per = w.n_positions * w.record_bytes
+        # layer-major, host[l][r][pos][W]: a layer's requests are adjacent
+        assert pool.host_records(2, 1).ctypes.data - a.ctypes.data == per
+        assert a.ctypes.data - pool.host_records(1, 0).ctypes.data == w.n_requests * per
+        assert pool.host_records(0, 0).ctypes.data + w.n_layers * w.n_requests * per == \
+            pool.host_records(w.n_requests - 1, w.n_layers - 1).ctypes.data + per
         a[:] = records.gen(w, 1, 1, np.arange(w.n_positions))
         assert np.array_equal(pool.host_records(1, 1)[17], records.gen(w, 1, 1, [17])[0])
 

@@ -66,6 +66,7 @@ L2_FLUSH_BYTES = 256 << 20
 HOST_ALLOC = {"auto": 0, "pinned": 1, "vmm": 2, "thp": 3}
 OVERLAP = {"auto": 0, "on": 1, "off": 2}
 CONT_STEPS, CONT_BLOCKS = 16, 3
+PREROLL_STEPS = 32  # untimed steps before the diagnostic passes of --prefetch-overlap
 
 # Counters of one steady-state resolve launch from an ncu capture
 # (profiles/resolve_kernel_tight_prefetch_full.md: tight_prefetch at full
@@ -1078,9 +1079,10 @@ def run_prefetch_overlap(args, w):
     the anchor's selection is known (ahead of the anchor's resolve), so plan
     and copy overlap the layers in between; the main stream waits for the
     copy before the GEMM ahead of the layer's resolve, which then consumes
-    the plan.  Four timings of the
-    same steps (CUDA events, L2 flushed before each step): the resolves
-    alone, the compute alone, both without prefetch, both with prefetch.
+    the plan.  After PREROLL_STEPS untimed steps and a reset, four timings
+    of the same steps (CUDA events, L2 flushed before each step): the
+    resolves alone, the compute alone, both without prefetch, both with
+    prefetch.
     The share of the resolves' own time hidden behind the compute is
     1 - (both - compute) / alone, with and without prefetch; `prefetch_gain`
     is what prefetch adds over resolves that already start under the
@@ -1186,6 +1188,12 @@ def run_prefetch_overlap(args, w):
                     main.wait_event(evs[l + 1])
                 compute()
 
+    # untimed pre-roll: on a freshly created huge-page pool the first tens of
+    # steps can stall, and the mode timed first would carry them
+    pool.reset()
+    for s in range(PREROLL_STEPS):
+        step(s % T, "off")
+    torch.cuda.synchronize()
     results = {}
     for mode in ("resolve", "compute", "off", "on"):
         pool.reset()
@@ -1237,6 +1245,7 @@ def run_prefetch_overlap(args, w):
         "attention": attn_res,
         "prefetch_kernels": kern,
         "steps": args.steps, "warmup": args.warmup,
+        "preroll_steps": PREROLL_STEPS,
     }
 
 

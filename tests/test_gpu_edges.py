@@ -173,9 +173,9 @@ def test_shapes(shape):
 
 
 @pytest.mark.parametrize("overlap", [hs.HS_OVERLAP_ON, hs.HS_OVERLAP_OFF])
-@pytest.mark.parametrize("cluster", ["1", "2", "4", "8"])
+@pytest.mark.parametrize("cluster", ["1", "2", "3", "4", "5", "7", "8"])
 def test_every_cluster_size(cluster, overlap, monkeypatch):
-    """Leader-only (1 CTA) and 1, 3, 7 followers give the same result, with
+    """Leader-only (1 CTA) and 1 to 7 followers give the same result, with
     launch overlap and without it (then the leader also fetches the misses
     of its own share of the selection)."""
     monkeypatch.setenv("HS_CLUSTER", cluster)
